@@ -1,0 +1,199 @@
+/*
+ * moe_experts.h - C ABI of the GB300 (sm_103a) routed top-k Mixture-of-Experts
+ * experts forward.
+ *
+ * What is computed (Hugging Face Transformers "Experts backends" page,
+ * introduction): for each token a router selects k experts; the token's
+ * hidden state goes through each selected expert's gated MLP (fused gate/up
+ * projection, SwiGLU, down projection; backends table, deepgemm_megamoe row,
+ * and the SonicMoE section's silu -> SwiGLU mapping) and the k results are
+ * summed with the routing weights.  Tokens are ordered by selected expert
+ * before the expert GEMMs (backends table, grouped_mm and deepgemm rows).  FP8
+ * experts carry float32 or UE8M0 block scales (paragraph after the backends
+ * table) and activations are quantised dynamically per row ("FP8 and FP4
+ * quantized experts" section).
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers named as device buffers must point to device memory of the
+ *     current CUDA device; the caller owns every buffer.  The library
+ *     allocates no device memory: scratch lives in a caller-provided
+ *     workspace sized by moe_workspace_size().
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     queued asynchronously on it; MOE_OK means "validated and launched".
+ *   - Row-major layouts everywhere.  bf16 buffers are passed as void*.
+ *   - Every device buffer must be 16-byte aligned.
+ *   - On a non-OK status nothing was launched (argument errors) or a CUDA
+ *     launch failed (MOE_ERR_CUDA); moe_last_error() gives a message.
+ *   - Errors are loud: an unsupported shape or format is rejected, never
+ *     computed approximately (the page's note on Blackwell scale formats:
+ *     fail "instead of silently corrupting the output").
+ */
+#ifndef MOE_EXPERTS_H
+#define MOE_EXPERTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer      */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape or format outside the supported set      */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed              */
+  MOE_ERR_TIMEOUT = 4,      /* a device-side bounded wait expired             */
+  MOE_ERR_WORKSPACE = 5     /* workspace missing or smaller than required     */
+} moe_status;
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1 } moe_wdtype;
+
+/* Block-scale format of FP8 weights (and of the dynamic activation scales,
+ * which always use the weights' format): MOE_SCALE_F32 stores float32 scales,
+ * MOE_SCALE_UE8M0 stores one byte b per block with scale 2^(b-127). */
+typedef enum { MOE_SCALE_NONE = 0, MOE_SCALE_F32 = 1, MOE_SCALE_UE8M0 = 2 } moe_scale_fmt;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+/* Message for the last non-OK status returned on this host thread. */
+const char* moe_last_error(void);
+
+/*
+ * moe_route - router top-k ("a router selects k experts", introduction).
+ *   logits   device fp32 [T, E]
+ *   topk_idx device int32 [T, k]  out: selected experts, slot j ordered by
+ *            descending logit, equal logits by ascending expert index
+ *   topk_w   device fp32 [T, k]   out: softmax over all E renormalised over
+ *            the k selected = exp(l_j - l_max) / sum over the selected; a row
+ *            whose largest logit is -inf gets 1/k in every slot
+ * Logits must not be NaN (not checked).  1 <= k <= min(E, 32), E <= 1024.
+ * T = 0 is a no-op.
+ */
+moe_status moe_route(const float* logits, int T, int E, int k,
+                     int32_t* topk_idx, float* topk_w, void* stream);
+
+/*
+ * moe_dispatch - order the T*k routing entries by expert (grouped_mm /
+ * deepgemm rows of the backends table).  Flat entry f = t*k + j.
+ *   counts   device int32 [E]    rows routed to each expert
+ *   offsets  device int32 [E+1]  exclusive scan of counts, offsets[E] = T*k
+ *   sorted_f device int32 [T*k]  row r of the expert-contiguous order holds
+ *            entry sorted_f[r]; within an expert entries ascend in f (stable)
+ *   row_of   device int32 [T*k]  inverse permutation
+ *   ws       device scratch of at least moe_dispatch_workspace_size() bytes
+ * topk_idx values must lie in [0, E); an out-of-range entry is reported as
+ * MOE_ERR_INVALID_ARG by the next moe_workspace_status() on this ws.
+ */
+size_t moe_dispatch_workspace_size(int T, int E, int k);
+moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k,
+                        int32_t* counts, int32_t* offsets, int32_t* sorted_f,
+                        int32_t* row_of, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_workspace_size - bytes of device scratch moe_experts_forward needs for
+ * these sizes and this weight type.
+ */
+size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
+
+/*
+ * moe_experts_forward - routed experts forward (introduction; gated MLP of
+ * the deepgemm_megamoe row; combine "with routing weights").
+ *   hidden      device bf16 [T, H]
+ *   topk_idx    device int32 [T, k], values in [0, E)
+ *   topk_w      device fp32 [T, k]
+ *   w_gate_up   device [E, 2I, H]: rows 0..I-1 of each expert are the gate
+ *               projection, rows I..2I-1 the up projection
+ *   w_down      device [E, H, I]
+ *   wdtype      MOE_W_BF16: weights are bf16, scales must be NULL and
+ *               sfmt MOE_SCALE_NONE.
+ *               MOE_W_FP8_E4M3: weights are e4m3 bytes with 128x128 block
+ *               scales scale_gate_up [E, 2I/128, H/128] and scale_down
+ *               [E, H/128, I/128], float32 or UE8M0 bytes per sfmt; the
+ *               activations (hidden rows and the SwiGLU output) are quantised
+ *               on the fly per row in 1x128 blocks with the same format.
+ *               There is no static activation scale.
+ *   out         device bf16 [T, H]: out[t] = sum_j topk_w[t,j] *
+ *               down(silu(gate x_t) * up x_t) of expert topk_idx[t,j],
+ *               accumulated in fp32 and rounded once to bf16
+ *   ws          device scratch, >= moe_workspace_size() bytes, 256-B aligned
+ * Requirements: H % 128 == 0, I % 128 == 0, 1 <= k <= min(E, 32),
+ * E <= 1024, T >= 0 (T = 0 is a no-op).  Other shapes: MOE_ERR_UNSUPPORTED.
+ * FP8 weights with MOE_SCALE_NONE: MOE_ERR_INVALID_ARG.
+ * Inputs are never written; out is fully overwritten.
+ * Calls that share one ws must be ordered (same stream or synchronised).
+ */
+moe_status moe_experts_forward(const void* hidden, int T, int H,
+                               const int32_t* topk_idx, const float* topk_w,
+                               int E, int k, int I,
+                               const void* w_gate_up, const void* w_down,
+                               moe_wdtype wdtype,
+                               const void* scale_gate_up, const void* scale_down,
+                               moe_scale_fmt sfmt,
+                               void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_quantize_fp8_blocks - quantise bf16 matrices into e4m3 codes with one
+ * scale per 128x128 block (the FP8 expert format of the "FP8 and FP4
+ * quantized experts" section).  Scale s = amax/448 (float32 division) for
+ * MOE_SCALE_F32, or the smallest power of two >= that quotient for
+ * MOE_SCALE_UE8M0 (stored as the biased exponent byte); amax = 0 gives
+ * s = 1; code = e4m3(x * (1/s)), round to nearest even, saturated to +-448.
+ *   w      device bf16 [nmat, rows, cols], rows % 128 == 0, cols % 128 == 0
+ *   q      device uint8 [nmat, rows, cols]
+ *   scale  device fp32 or uint8 [nmat, rows/128, cols/128]
+ */
+moe_status moe_quantize_fp8_blocks(const void* w, int nmat, int rows, int cols,
+                                   moe_scale_fmt sfmt, uint8_t* q, void* scale,
+                                   void* stream);
+
+/*
+ * moe_workspace_status - synchronise `stream`, read and clear the device
+ * error word at the head of `ws`.  Returns MOE_ERR_TIMEOUT if a bounded
+ * device wait expired in a kernel that used this workspace,
+ * MOE_ERR_INVALID_ARG if a kernel met an out-of-range expert index, MOE_OK
+ * otherwise.
+ */
+moe_status moe_workspace_status(void* ws, void* stream);
+
+/*
+ * moe_set_decode_rows - route forwards with T*k <= rows through the
+ * small-token decode path (weight streaming over the touched experts only,
+ * the page's "Decode-stage switching" idea); larger ones through the grouped
+ * tensor-core path.  rows < 0 restores the default.  Process-wide setting.
+ */
+void moe_set_decode_rows(int rows);
+int moe_get_decode_rows(void);
+
+/*
+ * Stage timing: between moe_profile_begin() and moe_profile_end() every
+ * launch of moe_experts_forward records a CUDA event pair on its stream
+ * around each stage.  moe_profile_end() synchronises those events and writes
+ * up to `n` entries: the summed milliseconds and launch count per stage
+ * (index = moe_stage); it returns the number of stages.  Not thread-safe.
+ */
+typedef enum {
+  MOE_STAGE_DISPATCH = 0, /* histogram, scan, permute, gather (+ quantise) */
+  MOE_STAGE_GEMM1 = 1,    /* gate/up projection + SwiGLU                   */
+  MOE_STAGE_GEMM2 = 2,    /* down projection + weighted combine             */
+  MOE_STAGE_FINISH = 3,   /* fp32 -> bf16 output                            */
+  MOE_STAGE_COUNT = 4
+} moe_stage;
+moe_status moe_profile_begin(void);
+int moe_profile_end(float* stage_ms, int* stage_launches, int n);
+
+/*
+ * moe_selftest_wait_timeout - launch one kernel that waits on a device
+ * barrier nothing will ever complete, with a wait limit of `limit_us`
+ * microseconds; the kernel gives up, records MOE_ERR_TIMEOUT in the error
+ * word at the head of `ws` and returns, leaving the context usable.  Used to
+ * test the timeout path without hanging a GPU.
+ */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EXPERTS_H */

@@ -1,0 +1,265 @@
+"""Routed top-k Mixture-of-Experts experts forward for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI declared in include/moe_experts.h.  It
+only checks and marshals arguments: every step of the forward runs in the
+library's CUDA kernels.  PyTorch provides device memory and the current
+stream.  There is no CPU or eager fallback: if the library is missing or no
+CUDA device is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
+    "experts_forward", "quantize_fp8_blocks", "workspace_status", "set_decode_rows",
+    "get_decode_rows", "profile_begin", "profile_end", "selftest_wait_timeout",
+    "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
+    "SCALE_UE8M0",
+]
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_WORKSPACE"}
+STAGES = ("dispatch", "gemm1", "gemm2", "finish")
+W_BF16, W_FP8_E4M3 = 0, 1
+SCALE_NONE, SCALE_F32, SCALE_UE8M0 = 0, 1, 2
+_SCALE_BY_NAME = {None: SCALE_NONE, "none": SCALE_NONE, "f32": SCALE_F32, "float": SCALE_F32,
+                  "ue8m0": SCALE_UE8M0}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_LIB = None
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "moe_version": ([], _I),
+    "moe_last_error": ([], ctypes.c_char_p),
+    "moe_route": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_dispatch_workspace_size": ([_I, _I, _I], _SZ),
+    "moe_dispatch": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "moe_workspace_size": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_experts_forward": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P,
+                             _SZ, _P], _I),
+    "moe_quantize_fp8_blocks": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_workspace_status": ([_P, _P], _I),
+    "moe_set_decode_rows": ([_I], None),
+    "moe_get_decode_rows": ([], _I),
+    "moe_profile_begin": ([], _I),
+    "moe_profile_end": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
+    "moe_selftest_wait_timeout": ([_P, _SZ, _I, _P], _I),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib(build_if_missing: bool = True):
+    """Load libmoe_gb300.so (building it in-tree first if it is absent)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.isfile(path):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library {path} is not built")
+        _build.build()
+    L = ctypes.CDLL(path)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _LIB = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        raise MoEError(status, lib().moe_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------------ router
+def route(logits: torch.Tensor, k: int, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Top-k routing of fp32 logits [T, E] -> (topk_idx int32 [T,k], topk_w fp32 [T,k])."""
+    _need_cuda(logits)
+    if logits.dtype != torch.float32 or logits.dim() != 2:
+        raise ValueError("logits must be fp32 [T, E]")
+    T, E = logits.shape
+    idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _stream(stream)))
+    return idx, w
+
+
+# ------------------------------------------------------------------ dispatch
+def dispatch_workspace_size(T: int, E: int, k: int) -> int:
+    return int(lib().moe_dispatch_workspace_size(T, E, k))
+
+
+def dispatch(topk_idx: torch.Tensor, E: int, stream=None):
+    """Expert-contiguous ordering -> (counts [E], offsets [E+1], sorted_f [T*k], row_of [T*k])."""
+    _need_cuda(topk_idx)
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be int32 [T, k]")
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_f = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T * k, dtype=torch.int32, device=dev)
+    nbytes = dispatch_workspace_size(T, E, k)
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    _check(lib().moe_dispatch(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets),
+                              _ptr(sorted_f), _ptr(row_of), _ptr(ws), nbytes, _stream(stream)))
+    _check(lib().moe_workspace_status(_ptr(ws), _stream(stream)))
+    return counts, offsets, sorted_f, row_of
+
+
+# ------------------------------------------------------------------ forward
+def workspace_size(T: int, H: int, I: int, E: int, k: int, wdtype: int = W_BF16) -> int:
+    return int(lib().moe_workspace_size(T, H, I, E, k, wdtype))
+
+
+class Workspace:
+    """Caller-owned device scratch for experts_forward, grown on demand.
+    The first 256 bytes hold the device error word; they start zeroed."""
+
+    def __init__(self, device="cuda"):
+        self.device = torch.device(device)
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 1024), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_DEFAULT_WS = {}
+
+
+def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                    w_gate_up: torch.Tensor, w_down: torch.Tensor,
+                    scale_gate_up: Optional[torch.Tensor] = None,
+                    scale_down: Optional[torch.Tensor] = None, scale_fmt=None,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
+                    stream=None) -> torch.Tensor:
+    """Routed experts forward -> bf16 [T, H].
+
+    hidden bf16 [T,H]; topk_idx int32 [T,k]; topk_w fp32 [T,k];
+    w_gate_up [E,2I,H] and w_down [E,H,I], bf16 or e4m3 bytes (uint8 or
+    float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0')."""
+    _need_cuda(hidden, topk_idx, topk_w, w_gate_up, w_down, scale_gate_up, scale_down, out)
+    T, H = hidden.shape
+    k = topk_idx.shape[1]
+    E, twoI, H2 = w_gate_up.shape
+    I = twoI // 2
+    if H2 != H or tuple(w_down.shape) != (E, H, I):
+        raise ValueError("weight shapes must be [E, 2I, H] and [E, H, I]")
+    if hidden.dtype != torch.bfloat16 or topk_idx.dtype != torch.int32 or topk_w.dtype != torch.float32:
+        raise ValueError("hidden bf16, topk_idx int32, topk_w fp32 expected")
+    fp8 = w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
+    wdtype = W_FP8_E4M3 if fp8 else W_BF16
+    if not fp8 and w_gate_up.dtype != torch.bfloat16:
+        raise ValueError("weights must be bf16 or e4m3 bytes")
+    sf = _SCALE_BY_NAME[scale_fmt] if not isinstance(scale_fmt, int) else scale_fmt
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
+    nbytes = workspace_size(T, H, I, E, k, wdtype)
+    if workspace is None:
+        key = hidden.device
+        workspace = _DEFAULT_WS.setdefault(key, Workspace(key))
+    ws = workspace.get(nbytes)
+    _check(lib().moe_experts_forward(
+        _ptr(hidden), T, H, _ptr(topk_idx), _ptr(topk_w), E, k, I, _ptr(w_gate_up),
+        _ptr(w_down), wdtype, _ptr(scale_gate_up), _ptr(scale_down), sf, _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
+
+
+def workspace_status(workspace, stream=None):
+    """Synchronise and raise MoEError if a kernel flagged an error in ws."""
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    _check(lib().moe_workspace_status(_ptr(ws), _stream(stream)))
+
+
+def default_workspace(device="cuda") -> Workspace:
+    d = torch.device(device)
+    if d.index is None:
+        d = torch.device("cuda", torch.cuda.current_device())
+    return _DEFAULT_WS.setdefault(d, Workspace(d))
+
+
+# ------------------------------------------------------------------ FP8
+def quantize_fp8_blocks(w: torch.Tensor, scale_fmt: str = "f32", stream=None):
+    """bf16 [..., R, C] -> (e4m3 codes uint8 [..., R, C], scales [..., R/128, C/128]
+    as fp32 ('f32') or uint8 exponent bytes ('ue8m0'))."""
+    _need_cuda(w)
+    if w.dtype != torch.bfloat16:
+        raise ValueError("w must be bf16")
+    *lead, R, C = w.shape
+    nmat = 1
+    for d in lead:
+        nmat *= d
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sf = _SCALE_BY_NAME[scale_fmt]
+    sdt = torch.uint8 if sf == SCALE_UE8M0 else torch.float32
+    s = torch.empty(*lead, R // 128 if R % 128 == 0 else 0, C // 128 if C % 128 == 0 else 0,
+                    dtype=sdt, device=w.device)
+    _check(lib().moe_quantize_fp8_blocks(_ptr(w), nmat, R, C, sf, _ptr(q), _ptr(s),
+                                         _stream(stream)))
+    return q, s
+
+
+# ------------------------------------------------------------------ control
+def set_decode_rows(rows: int):
+    lib().moe_set_decode_rows(int(rows))
+
+
+def get_decode_rows() -> int:
+    return int(lib().moe_get_decode_rows())
+
+
+def profile_begin():
+    _check(lib().moe_profile_begin())
+
+
+def profile_end():
+    """-> {stage: (total_ms, launches)} for the forwards since profile_begin()."""
+    n = len(STAGES)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    lib().moe_profile_end(ms, cnt, n)
+    return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the status that
+    moe_workspace_status reports afterwards (expected MOE_ERR_TIMEOUT)."""
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    _check(lib().moe_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)))
+    return int(lib().moe_workspace_status(_ptr(ws), _stream(stream)))

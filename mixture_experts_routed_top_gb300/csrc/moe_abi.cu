@@ -1,0 +1,437 @@
+// C-ABI entry points: argument validation, workspace layout, tensor-map
+// construction and the launch sequence of the routed experts forward.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int g_decode_rows = -1;  // < 0: default
+
+// ----------------------------------------------------------- workspace map
+struct WsLayout {
+  size_t counts, offsets, tile_pref, touched, sorted_f, row_of, blk_counts;
+  size_t xa, xa_scale, hb, hb_scale, out32;
+  size_t total;
+};
+
+WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
+  WsLayout L{};
+  const long n = T * k;
+  const long nchunks = n ? (n + kDispatchChunk - 1) / kDispatchChunk : 0;
+  size_t off = sizeof(WsHeader);
+  auto take = [&](size_t bytes) {
+    size_t at = align_up(off, 1024);
+    off = at + bytes;
+    return at;
+  };
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.tile_pref = take((E + 1) * 4);
+  L.touched = take((E + 1) * 4);
+  L.sorted_f = take(n * 4);
+  L.row_of = take(n * 4);
+  L.blk_counts = take(nchunks * E * 4);
+  const size_t esz = fp8 ? 1 : 2;
+  L.xa = take(n * H * esz);
+  L.xa_scale = take(fp8 ? n * (H / 128) * 4 : 0);
+  L.hb = take(n * I * esz);
+  L.hb_scale = take(fp8 ? n * (I / 128) * 4 : 0);
+  L.out32 = take(T * H * 4);
+  L.total = align_up(off, 1024);
+  return L;
+}
+
+size_t dispatch_ws_bytes(long T, long E, long k) {
+  const long n = T * k;
+  const long nchunks = n ? (n + kDispatchChunk - 1) / kDispatchChunk : 0;
+  size_t off = align_up(sizeof(WsHeader), 1024);
+  off = align_up(off + (E + 1) * 4, 1024);  // tile prefix
+  off = align_up(off + (E + 1) * 4, 1024);  // touched list
+  off = align_up(off + nchunks * E * 4, 1024);
+  return off;
+}
+
+// ----------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major [outer, inner] matrix, box = 128 rows x 128 bytes, 128-byte
+// swizzle, out-of-range rows read as zero.
+moe_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                    uint64_t inner, uint64_t outer) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+// ----------------------------------------------------------- stage timing
+struct Profiler {
+  bool on = false;
+  struct Rec {
+    int stage;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+Profiler g_prof;
+std::mutex g_prof_mu;
+
+struct StageScope {
+  cudaStream_t s;
+  int stage;
+  cudaEvent_t b = nullptr;
+  StageScope(cudaStream_t s_, int st) : s(s_), stage(st) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaEvent_t a = g_prof.get();
+    b = g_prof.get();
+    cudaEventRecord(a, s);
+    g_prof.recs.push_back({stage, a, b});
+  }
+  ~StageScope() {
+    if (b) cudaEventRecord(b, s);
+  }
+};
+
+}  // namespace
+
+// =========================================================== exported API
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+void moe_set_decode_rows(int rows) { g_decode_rows = rows; }
+int moe_get_decode_rows(void) { return g_decode_rows < 0 ? 0 : g_decode_rows; }
+
+moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
+                     void* stream) {
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "moe_route: T < 0");
+  if (E < 1 || E > kMaxE) return fail(MOE_ERR_UNSUPPORTED, "moe_route: E must be in [1, %d]", kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_route: k must be in [1, min(E, %d)]", kMaxK);
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "moe_route: null pointer");
+  if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: misaligned pointer");
+  cudaError_t e = launch_route(logits, T, E, k, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route launch");
+  return MOE_OK;
+}
+
+size_t moe_dispatch_workspace_size(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  return dispatch_ws_bytes(T, E, k);
+}
+
+moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, int32_t* counts,
+                        int32_t* offsets, int32_t* sorted_f, int32_t* row_of, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: T < 0");
+  if (E < 1 || E > kMaxE) return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch: E must be in [1, %d]", kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch: k must be in [1, min(E, %d)]", kMaxK);
+  if (static_cast<long>(T) * k > 0x7FFFFFFFL)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch: T*k exceeds int32");
+  if (!counts || !offsets || !ws || (T > 0 && (!topk_idx || !sorted_f || !row_of)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: null pointer");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: ws must be 256-byte aligned");
+  const size_t need = dispatch_ws_bytes(T, E, k);
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace %zu < %zu bytes", ws_bytes, need);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const long n = static_cast<long>(T) * k;
+  DispatchBufs d;
+  size_t off = align_up(sizeof(WsHeader), 1024);
+  d.err = reinterpret_cast<int*>(w);
+  d.counts = counts;
+  d.offsets = offsets;
+  d.tile_pref = reinterpret_cast<int*>(w + off);
+  off = align_up(off + (E + 1) * 4, 1024);
+  d.touched = reinterpret_cast<int*>(w + off);
+  off = align_up(off + (E + 1) * 4, 1024);
+  d.blk_counts = reinterpret_cast<int*>(w + off);
+  d.sorted_f = sorted_f;
+  d.row_of = row_of;
+  (void)n;
+  cudaError_t e = launch_dispatch(topk_idx, T, E, k, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_dispatch launch");
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  return ws_layout(T, H, I, E, k, wdtype == MOE_W_FP8_E4M3).total;
+}
+
+moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* topk_idx,
+                               const float* topk_w, int E, int k, int I, const void* w_gate_up,
+                               const void* w_down, moe_wdtype wdtype, const void* scale_gate_up,
+                               const void* scale_down, moe_scale_fmt sfmt, void* out, void* ws,
+                               size_t ws_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T < 0 || H < 1 || I < 1) return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: bad sizes");
+  if (E < 1 || E > kMaxE)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: E must be in [1, %d]", kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: k must be in [1, min(E, %d)]", kMaxK);
+  if (H % 128 || I % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: H and I must be multiples of 128");
+  if (static_cast<long>(T) * k > 0x7FFFFFFFL)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: T*k exceeds int32");
+  const bool fp8 = wdtype == MOE_W_FP8_E4M3;
+  if (wdtype != MOE_W_BF16 && !fp8)
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: unknown weight dtype %d", (int)wdtype);
+  if (fp8) {
+    if (sfmt != MOE_SCALE_F32 && sfmt != MOE_SCALE_UE8M0)
+      return fail(MOE_ERR_INVALID_ARG,
+                  "moe_experts_forward: FP8 weights need float32 or UE8M0 block scales");
+    if (!scale_gate_up || !scale_down)
+      return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP8 weights need scale buffers");
+  } else if (sfmt != MOE_SCALE_NONE || scale_gate_up || scale_down) {
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: bf16 weights take no scales");
+  }
+  if (T == 0) return MOE_OK;
+  if (!hidden || !topk_idx || !topk_w || !w_gate_up || !w_down || !out || !ws)
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: null pointer");
+  const void* ptrs[] = {hidden, topk_idx, topk_w, w_gate_up, w_down, out};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16)) return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: buffers must be 16-byte aligned");
+  if (!aligned(ws, 256))
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: ws must be 256-byte aligned");
+  const WsLayout L = ws_layout(T, H, I, E, k, fp8);
+  if (ws_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "moe_experts_forward: workspace %zu < %zu bytes", ws_bytes,
+                L.total);
+  if (fp8) return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: FP8 path not built yet");
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const long n = static_cast<long>(T) * k;
+  DispatchBufs d;
+  d.err = reinterpret_cast<int*>(w);
+  d.counts = reinterpret_cast<int*>(w + L.counts);
+  d.offsets = reinterpret_cast<int*>(w + L.offsets);
+  d.tile_pref = reinterpret_cast<int*>(w + L.tile_pref);
+  d.touched = reinterpret_cast<int*>(w + L.touched);
+  d.sorted_f = reinterpret_cast<int*>(w + L.sorted_f);
+  d.row_of = reinterpret_cast<int*>(w + L.row_of);
+  d.blk_counts = reinterpret_cast<int*>(w + L.blk_counts);
+  void* xa = w + L.xa;
+  void* hb = w + L.hb;
+  float* out32 = reinterpret_cast<float*>(w + L.out32);
+
+  CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
+  moe_status st;
+  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n)) != MOE_OK) return st;
+  if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
+                     static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+    return st;
+  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n)) != MOE_OK) return st;
+  if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
+                     static_cast<uint64_t>(E) * H)) != MOE_OK)
+    return st;
+
+  cudaError_t e;
+  {
+    StageScope sc(s, MOE_STAGE_DISPATCH);
+    if ((e = launch_dispatch(topk_idx, T, E, k, d, s)) != cudaSuccess) return cuda_fail(e, "dispatch");
+    if ((e = launch_gather_bf16(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), xa,
+                                s)) != cudaSuccess)
+      return cuda_fail(e, "gather");
+    if ((e = cudaMemsetAsync(out32, 0, static_cast<size_t>(T) * H * 4, s)) != cudaSuccess)
+      return cuda_fail(e, "memset");
+  }
+  const int sms = num_sms();
+  GroupedGemmArgs g{};
+  g.offsets = d.offsets;
+  g.tile_pref = d.tile_pref;
+  g.E = E;
+  g.I = I;
+  g.H = H;
+  g.k = k;
+  g.err = d.err;
+  g.h_out = hb;
+  g.out32 = out32;
+  g.sorted_f = d.sorted_f;
+  g.topk_w = topk_w;
+  // upper bound on tiles: sum_e ceil(M_e/128) <= n/128 + E
+  const long mtiles_max = n / kBM + E;
+  {
+    StageScope sc(s, MOE_STAGE_GEMM1);
+    g.tm_a = &tm_x;
+    g.tm_b = &tm_wgu;
+    g.K = H;
+    g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
+    if ((e = launch_gemm1_bf16(g, s)) != cudaSuccess) return cuda_fail(e, "gemm1");
+  }
+  {
+    StageScope sc(s, MOE_STAGE_GEMM2);
+    g.tm_a = &tm_h;
+    g.tm_b = &tm_wd;
+    g.K = I;
+    const int bn = (H % 256 == 0) ? 256 : 128;
+    g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / bn)));
+    if ((e = launch_gemm2_bf16(g, s)) != cudaSuccess) return cuda_fail(e, "gemm2");
+  }
+  {
+    StageScope sc(s, MOE_STAGE_FINISH);
+    if ((e = launch_to_bf16(out32, out, static_cast<long>(T) * H, s)) != cudaSuccess)
+      return cuda_fail(e, "to_bf16");
+  }
+  return MOE_OK;
+}
+
+moe_status moe_quantize_fp8_blocks(const void* wsrc, int nmat, int rows, int cols,
+                                   moe_scale_fmt sfmt, uint8_t* q, void* scale, void* stream) {
+  if (nmat < 0 || rows < 0 || cols < 0)
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp8_blocks: negative size");
+  if (rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_quantize_fp8_blocks: rows and cols must be multiples of 128");
+  if (sfmt != MOE_SCALE_F32 && sfmt != MOE_SCALE_UE8M0)
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp8_blocks: scale format must be F32 or UE8M0");
+  if (static_cast<long>(nmat) * rows * cols == 0) return MOE_OK;
+  if (!wsrc || !q || !scale) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp8_blocks: null pointer");
+  if (!aligned(wsrc, 16) || !aligned(q, 16) || !aligned(scale, 4))
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp8_blocks: misaligned pointer");
+  cudaError_t e = launch_quantize_blocks(wsrc, nmat, rows, cols, sfmt == MOE_SCALE_UE8M0, q, scale,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_quantize_fp8_blocks launch");
+  return MOE_OK;
+}
+
+moe_status moe_workspace_status(void* ws, void* stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "moe_workspace_status: null workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int err = 0;
+  cudaError_t e = cudaMemcpyAsync(&err, ws, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_workspace_status");
+  if (err) {
+    const int zero = 0;
+    e = cudaMemcpyAsync(ws, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_workspace_status clear");
+    if (err & (ERR_TIMEOUT_PRODUCER | ERR_TIMEOUT_MMA | ERR_TIMEOUT_EPILOGUE | ERR_TIMEOUT_SELFTEST))
+      return fail(MOE_ERR_TIMEOUT, "device wait timed out (error word 0x%x)", err);
+    return fail(MOE_ERR_INVALID_ARG, "kernel met an out-of-range expert index (error word 0x%x)", err);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_profile_begin(void) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof.recs) {
+    g_prof.pool.push_back(r.a);
+    g_prof.pool.push_back(r.b);
+  }
+  g_prof.recs.clear();
+  g_prof.on = true;
+  return MOE_OK;
+}
+
+int moe_profile_end(float* stage_ms, int* stage_launches, int n) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof.on = false;
+  std::vector<float> ms(MOE_STAGE_COUNT, 0.f);
+  std::vector<int> cnt(MOE_STAGE_COUNT, 0);
+  for (auto& r : g_prof.recs) {
+    cudaEventSynchronize(r.b);
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      ms[r.stage] += t;
+      cnt[r.stage] += 1;
+    }
+    g_prof.pool.push_back(r.a);
+    g_prof.pool.push_back(r.b);
+  }
+  g_prof.recs.clear();
+  for (int i = 0; i < n && i < MOE_STAGE_COUNT; ++i) {
+    if (stage_ms) stage_ms[i] = ms[i];
+    if (stage_launches) stage_launches[i] = cnt[i];
+  }
+  return MOE_STAGE_COUNT;
+}
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int limit_us, void* stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader) || !aligned(ws, 256))
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: bad workspace");
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: limit_us must be in [1, 1e6]");
+  cudaError_t e = launch_selftest_wait(static_cast<int*>(ws), limit_us, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_selftest_wait_timeout launch");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_experts.h"
+
+namespace moe {
+
+// Error word bits written by kernels into the head of the workspace.
+enum : int {
+  ERR_TIMEOUT_PRODUCER = 1,
+  ERR_TIMEOUT_MMA = 2,
+  ERR_TIMEOUT_EPILOGUE = 4,
+  ERR_TIMEOUT_SELFTEST = 8,
+  ERR_BAD_INDEX = 16,
+};
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kDispatchChunk = 2048;   // routing entries per histogram/permute block
+constexpr int kBM = 128;               // token rows per grouped-GEMM tile
+
+// Device-side error word block at the head of every workspace.
+struct WsHeader {
+  int err;
+  int pad[63];
+};
+
+// Pointers into the dispatch part of a workspace.
+struct DispatchBufs {
+  int* err;
+  int* counts;       // [E]
+  int* offsets;      // [E+1]
+  int* tile_pref;    // [E+1] prefix of ceil(count/128)
+  int* sorted_f;     // [T*k]
+  int* row_of;       // [T*k]
+  int* blk_counts;   // [nchunks * E]
+  int* touched;      // [E+1]: touched[0] = n, then expert ids ascending
+};
+
+inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Kernel launchers (return cudaGetLastError()).
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         cudaStream_t s);
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const DispatchBufs& d,
+                            cudaStream_t s);
+cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,
+                               const int* nvalid, int rows, void* x_perm, cudaStream_t s);
+cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
+                              const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
+                              cudaStream_t s);
+cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s);
+cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, bool ue8m0,
+                                   uint8_t* q, void* scale, cudaStream_t s);
+cudaError_t launch_selftest_wait(int* err, int limit_us, cudaStream_t s);
+
+// Grouped tensor-core GEMMs.
+struct GroupedGemmArgs {
+  const CUtensorMap* tm_a;   // activations [rows, K], box 128 rows
+  const CUtensorMap* tm_b;   // weights [E * Nw, K], box 128 rows
+  const int* offsets;        // [E+1]
+  const int* tile_pref;      // [E+1]
+  int E, K, I, H, k;
+  int* err;
+  // gate/up + SwiGLU epilogue
+  void* h_out;               // bf16 [rows, I]
+  // down + combine epilogue
+  float* out32;              // [T, H]
+  const int* sorted_f;
+  const float* topk_w;
+  int num_sms;
+};
+cudaError_t launch_gemm1_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+
+}  // namespace moe

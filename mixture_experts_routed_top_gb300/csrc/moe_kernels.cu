@@ -1,0 +1,418 @@
+// Router, dispatch, gather, output conversion and FP8 block quantisation
+// kernels (everything except the grouped tensor-core GEMMs).
+#include <cuda_fp8.h>
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+// ============================================================== router
+// One warp per token.  Lane l holds logits l, l+32, ... in registers; k
+// rounds of a warp-wide arg-max pick the experts in slot order (descending
+// logit, ties to the lower expert index), then the kept logits go through a
+// softmax relative to the largest one.  Selection uses only comparisons of
+// the fp32 logits, so the chosen indices are exact.
+template <int NPL>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int k, int32_t* __restrict__ topk_idx,
+                                                    float* __restrict__ topk_w) {
+  const int lane = threadIdx.x & 31;
+  const long t = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  float v[NPL];
+  uint32_t used = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+    if (e >= E) used |= 1u << i;
+  }
+  float my_v = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX;  // INT_MAX = no candidate
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (!((used >> i) & 1u) && (be == INT_MAX || v[i] > bv)) {
+        bv = v[i];
+        be = lane + 32 * i;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      const bool take = (oe != INT_MAX) &&
+                        (be == INT_MAX || ov > bv || (ov == bv && oe < be));
+      if (take) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) used |= 1u << (be >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const bool dead = isinf(top) && top < 0.f;
+  float ex = (lane < k && !dead) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    topk_idx[t * k + lane] = my_e;
+    topk_w[t * k + lane] = dead ? 1.0f / static_cast<float>(k) : ex / sum;
+  }
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int npl = ceil_div(E, 32);
+  dim3 block(256), grid(ceil_div(static_cast<long>(T) * 32, 256));
+  if (npl <= 1) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  else if (npl <= 2) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  else if (npl <= 4) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  else if (npl <= 8) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  else if (npl <= 16) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  return cudaGetLastError();
+}
+
+// ============================================================== dispatch
+// (1) per-chunk expert histograms, (2) one-block scan that turns them into
+// per-chunk write bases plus counts/offsets/tile prefix/touched list,
+// (3) per-chunk stable placement, one warp walking its chunk in order.
+// Out-of-range expert ids are skipped everywhere and flagged in the error
+// word, so no later kernel ever indexes with them.
+
+__global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ idx,
+                                                             long n, int E, int* blk_counts,
+                                                             int* err) {
+  __shared__ int hist[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const long base = static_cast<long>(blockIdx.x) * kDispatchChunk;
+  const long end = min(base + kDispatchChunk, n);
+  bool bad = false;
+  for (long f = base + threadIdx.x; f < end; f += blockDim.x) {
+    const int e = __ldg(idx + f);
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(err, ERR_BAD_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blk_counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
+}
+
+// Exclusive scan of one value per thread over a block of 1024 threads.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int ws = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws += y;
+    }
+    s_warp[lane] = ws - w;  // exclusive prefix of warp totals
+    if (lane == 31) s_warp[32] = ws;
+  }
+  __syncthreads();
+  const int res = s_warp[warp] + x - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks, int* blk_counts,
+                                                             int* counts, int* offsets,
+                                                             int* tile_pref, int* touched) {
+  __shared__ int s_warp[33];
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+    for (int b = 0; b < nchunks; ++b) {
+      const long i = static_cast<long>(b) * E + e;
+      const int v = blk_counts[i];
+      blk_counts[i] = c;
+      c += v;
+    }
+  }
+  const int tiles = (c + kBM - 1) / kBM;
+  const int tch = c > 0 ? 1 : 0;
+  int tot_c, tot_t, tot_h;
+  const int ex_c = block_exclusive_scan(c, s_warp, &tot_c);
+  const int ex_t = block_exclusive_scan(tiles, s_warp, &tot_t);
+  const int ex_h = block_exclusive_scan(tch, s_warp, &tot_h);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = ex_c;
+    tile_pref[e] = ex_t;
+    if (tch) touched[1 + ex_h] = e;
+    for (int b = 0; b < nchunks; ++b) blk_counts[static_cast<long>(b) * E + e] += ex_c;
+  }
+  if (e == 0) {
+    offsets[E] = tot_c;
+    tile_pref[E] = tot_t;
+    touched[0] = tot_h;
+  }
+}
+
+__global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __restrict__ idx, long n,
+                                                            int E, const int* blk_base,
+                                                            int* sorted_f, int* row_of) {
+  __shared__ int cursor[kMaxE];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cursor[e] = blk_base[static_cast<long>(blockIdx.x) * E + e];
+  __syncwarp();
+  const long base = static_cast<long>(blockIdx.x) * kDispatchChunk;
+  const long end = min(base + kDispatchChunk, n);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (long f0 = base; f0 < end; f0 += 32) {
+    const long f = f0 + lane;
+    int e = (f < end) ? __ldg(idx + f) : -1;
+    if (e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int pos = -1;
+    if (e >= 0) {
+      pos = cursor[e] + __popc(peers & lt);
+      sorted_f[pos] = static_cast<int>(f);
+    }
+    if (f < end) row_of[f] = pos;
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) cursor[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const DispatchBufs& d,
+                            cudaStream_t s) {
+  const long n = static_cast<long>(T) * k;
+  const int nchunks = n ? ceil_div(n, kDispatchChunk) : 0;
+  if (nchunks) {
+    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, n, E, d.blk_counts, d.err);
+  }
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(E, nchunks, d.blk_counts, d.counts, d.offsets,
+                                          d.tile_pref, d.touched);
+  if (nchunks) {
+    dispatch_place_kernel<<<nchunks, 32, 0, s>>>(topk_idx, n, E, d.blk_counts, d.sorted_f,
+                                                 d.row_of);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================== gather
+// X_perm[r, :] = hidden[sorted_f[r] / k, :] for the rows the dispatch placed
+// (r < offsets[E]); one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restrict__ hidden, int H8,
+                                                          int k, const int* __restrict__ sorted_f,
+                                                          const int* __restrict__ nvalid, int rows,
+                                                          uint4* __restrict__ xperm) {
+  const int lane = threadIdx.x & 31;
+  const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (r >= rows || r >= *nvalid) return;
+  const long t = __ldg(sorted_f + r) / k;
+  const uint4* src = hidden + t * H8;
+  uint4* dst = xperm + r * H8;
+  for (int c = lane; c < H8; c += 32) dst[c] = __ldg(src + c);
+}
+
+cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,
+                               const int* nvalid, int rows, void* x_perm, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  gather_bf16_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4*>(hidden), H / 8, k,
+                                                       sorted_f, nvalid, rows,
+                                                       static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+// ============================================================== FP8 helpers
+// Scale of one block from its absolute maximum: amax/448 (IEEE fp32
+// division) or the smallest power of two >= that quotient; amax = 0 -> 1.
+// Returns the scale value and its stored form (fp32 bits or exponent byte).
+__device__ __forceinline__ float block_scale(float amax, bool ue8m0, uint32_t* stored) {
+  if (amax == 0.f) {
+    *stored = ue8m0 ? 127u : __float_as_uint(1.0f);
+    return 1.0f;
+  }
+  const float q = amax / 448.0f;
+  if (!ue8m0) {
+    *stored = __float_as_uint(q);
+    return q;
+  }
+  const uint32_t bits = __float_as_uint(q);
+  int b = static_cast<int>((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+  b = b > 254 ? 254 : b;
+  *stored = static_cast<uint32_t>(b);
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(b) << 23);
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Gather + dynamic 1x128 activation quantisation: one warp per row, each
+// lane owns 4 consecutive elements of every 128-wide block.
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint2* __restrict__ hidden, int H,
+                                                         int k, const int* __restrict__ sorted_f,
+                                                         const int* __restrict__ nvalid, int rows,
+                                                         bool ue8m0, uint32_t* __restrict__ xq,
+                                                         void* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (r >= rows || r >= *nvalid) return;
+  const long t = __ldg(sorted_f + r) / k;
+  const int nb = H / 128;
+  const uint2* src = hidden + t * (H / 4);
+  uint32_t* dst = xq + r * (H / 4);
+  for (int b = 0; b < nb; ++b) {
+    const uint2 raw = __ldg(src + b * 32 + lane);
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const float x0 = __low2float(p0), x1 = __high2float(p0);
+    const float x2 = __low2float(p1), x3 = __high2float(p1);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
+    uint32_t stored;
+    const float sc = block_scale(amax, ue8m0, &stored);
+    const float inv = 1.0f / sc;
+    const uint32_t lo = e4m3x2(x0 * inv, x1 * inv);
+    const uint32_t hi = e4m3x2(x2 * inv, x3 * inv);
+    dst[b * 32 + lane] = lo | (hi << 16);
+    if (lane == 0) {
+      if (ue8m0) static_cast<uint8_t*>(xs)[r * nb + b] = static_cast<uint8_t>(stored);
+      else static_cast<uint32_t*>(xs)[r * nb + b] = stored;
+    }
+  }
+}
+
+cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
+                              const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
+                              cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  gather_fp8_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint2*>(hidden), H, k,
+                                                      sorted_f, nvalid, rows, ue8m0,
+                                                      reinterpret_cast<uint32_t*>(xq), xs);
+  return cudaGetLastError();
+}
+
+// ============================================================== finish
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src,
+                                                      uint2* __restrict__ dst, long n4) {
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldg(src + i);
+    dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s) {
+  const long n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  const long want = (n4 + 255) / 256;
+  const int grid = static_cast<int>(want < 152L * 16 ? want : 152L * 16);
+  to_bf16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+                                      reinterpret_cast<uint2*>(dst), n4);
+  return cudaGetLastError();
+}
+
+// ============================================================== weight quantiser
+// One 256-thread block per 128x128 block: amax, scale, codes.  Thread t
+// covers row t/2, columns (t%2)*64 .. +63.
+__global__ void __launch_bounds__(256) quantize_blocks_kernel(const uint4* __restrict__ w, int rows,
+                                                              int cols, bool ue8m0,
+                                                              uint2* __restrict__ q,
+                                                              void* __restrict__ scale) {
+  __shared__ float s_max[8];
+  const int nbc = cols / 128, nbr = rows / 128;
+  const long blk = blockIdx.x;  // over nmat * nbr * nbc
+  const long mat = blk / (static_cast<long>(nbr) * nbc);
+  const int rb = static_cast<int>((blk / nbc) % nbr), cb = static_cast<int>(blk % nbc);
+  const int row = rb * 128 + (threadIdx.x >> 1);
+  const int col0 = cb * 128 + (threadIdx.x & 1) * 64;
+  const long base = (mat * rows + row) * static_cast<long>(cols) + col0;  // element index
+  uint4 v[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = __ldg(w + base / 8 + i);
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      amax = fmaxf(amax, fmaxf(fabsf(__low2float(p[j])), fabsf(__high2float(p[j]))));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = s_max[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_max[i]);
+  uint32_t stored;
+  const float sc = block_scale(amax, ue8m0, &stored);
+  const float inv = 1.0f / sc;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = e4m3x2(__low2float(p[j]) * inv, __high2float(p[j]) * inv);
+    q[base / 8 + i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  }
+  if (threadIdx.x == 0) {
+    if (ue8m0) static_cast<uint8_t*>(scale)[blk] = static_cast<uint8_t>(stored);
+    else static_cast<uint32_t*>(scale)[blk] = stored;
+  }
+}
+
+cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, bool ue8m0,
+                                   uint8_t* q, void* scale, cudaStream_t s) {
+  const long nblk = static_cast<long>(nmat) * (rows / 128) * (cols / 128);
+  if (nblk == 0) return cudaSuccess;
+  quantize_blocks_kernel<<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+      static_cast<const uint4*>(w), rows, cols, ue8m0, reinterpret_cast<uint2*>(q), scale);
+  return cudaGetLastError();
+}
+
+// ============================================================== self-test
+// Waits on an mbarrier that nothing completes; the bounded wait must give up
+// after limit_us, set the error word and return.
+__global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x != 0) return;
+  abort = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  mbar_wait_bounded(smem_u32(&bar), 0, &abort, err, ERR_TIMEOUT_SELFTEST, limit_ns);
+}
+
+cudaError_t launch_selftest_wait(int* err, int limit_us, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

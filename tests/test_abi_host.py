@@ -1,0 +1,76 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/moe_experts.h declares, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_experts.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mixture_experts_routed_top_gb300 import build, lib
+    build.build()
+    return lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("moe_route", "moe_dispatch", "moe_experts_forward", "moe_workspace_size",
+              "moe_quantize_fp8_blocks", "moe_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_version_and_sizes(L):
+    assert L.moe_version() >= 100
+    a = L.moe_workspace_size(64, 128, 256, 8, 2, 0)
+    b = L.moe_workspace_size(4096, 2048, 1408, 60, 4, 0)
+    assert 0 < a < b
+    # x_perm (T*k*H bf16) + h (T*k*I bf16) + fp32 accumulator dominate
+    assert b >= 4096 * 4 * (2048 + 1408) * 2 + 4096 * 2048 * 4
+    f8 = L.moe_workspace_size(4096, 2048, 1408, 60, 4, 1)
+    assert f8 < b
+    assert L.moe_workspace_size(-1, 128, 128, 8, 2, 0) == 0
+
+
+def test_argument_errors_without_device(L):
+    nul = ctypes.c_void_p(0)
+    assert L.moe_route(nul, 4, 0, 1, nul, nul, nul) == 2          # E < 1
+    assert L.moe_route(nul, 4, 8, 9, nul, nul, nul) == 2          # k > E
+    assert L.moe_route(nul, 4, 2000, 2, nul, nul, nul) == 2       # E > 1024
+    assert L.moe_route(nul, 4, 8, 2, nul, nul, nul) == 1          # null pointers
+    assert b"null" in L.moe_last_error()
+    assert L.moe_route(nul, 0, 8, 2, nul, nul, nul) == 0          # T = 0 no-op
+    f = L.moe_experts_forward
+    # H not a multiple of 128
+    assert f(nul, 4, 100, nul, nul, 8, 2, 128, nul, nul, 0, nul, nul, 0, nul, nul, 0, nul) == 2
+    # FP8 weights without a scale format
+    assert f(nul, 4, 128, nul, nul, 8, 2, 128, nul, nul, 1, nul, nul, 0, nul, nul, 0, nul) == 1
+    # bf16 weights with a scale format
+    assert f(nul, 4, 128, nul, nul, 8, 2, 128, nul, nul, 0, nul, nul, 1, nul, nul, 0, nul) == 1
+    # workspace too small (checked before any launch); fake aligned pointers
+    p = ctypes.c_void_p(1 << 20)
+    assert f(p, 4, 128, p, p, 8, 2, 128, p, p, 0, nul, nul, 0, p, p, 16, nul) == 5
+    assert L.moe_quantize_fp8_blocks(nul, 1, 100, 128, 1, nul, nul, nul) == 2
+    assert L.moe_quantize_fp8_blocks(nul, 1, 128, 128, 0, nul, nul, nul) == 1
+
+
+def test_decode_rows_setting(L):
+    L.moe_set_decode_rows(77)
+    assert L.moe_get_decode_rows() == 77
+    L.moe_set_decode_rows(-1)

@@ -1,0 +1,217 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing indices, counts, offsets and the permutation must match bit for bit;
+routing weights within 2e-6 relative; the bf16 forward within
+max|err| / rms(ref) <= 2e-2 (the float tolerance the workload definition
+states).  Sizes span several 128-row tiles with ragged tails, empty experts,
+one overloaded expert, T = 1, and the full workload sizes on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from workloads import MoEShape, make_inputs, shape_for
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_routed_top_gb300 as m
+    m.lib()
+    return m
+
+
+def _to_np(t):
+    return t.detach().cpu().float().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
+
+
+# ----------------------------------------------------------------- router
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (4096, 60, 4), (1000, 256, 8), (3, 1024, 32),
+                                   (33, 33, 32), (5, 1, 1), (17, 40, 7)])
+def test_route_parity(moe, T, E, k):
+    g = torch.Generator().manual_seed(T * 7 + E)
+    logits = torch.randn(T, E, generator=g)
+    logits[: T // 3, E // 2] = logits[: T // 3, 0]          # exact ties
+    if T > 2:
+        logits[1] = 0.25                                    # all equal
+        logits[2, : max(1, E - k)] = float("-inf")          # -inf entries
+    idx, w = moe.route(logits.cuda(), k)
+    ref_idx, ref_w = O.route(logits.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
+def test_route_all_neg_inf_row(moe):
+    logits = torch.full((2, 6), float("-inf"))
+    logits[1, 4] = 1.0
+    idx, w = moe.route(logits.cuda(), 3)
+    ref_idx, ref_w = O.route(logits.numpy(), 3)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=1e-6)
+
+
+def test_route_empty(moe):
+    idx, w = moe.route(torch.empty(0, 8, device="cuda"), 2)
+    assert idx.shape == (0, 2)
+
+
+# ----------------------------------------------------------------- dispatch
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (4096, 60, 4), (5000, 256, 8), (1, 4, 4),
+                                   (700, 1024, 3), (2049, 2, 1)])
+def test_dispatch_parity(moe, T, E, k):
+    g = torch.Generator().manual_seed(T + E + k)
+    logits = torch.randn(T, E, generator=g)
+    logits[:, 0] += 2.0                                      # one popular expert
+    if E > 3:
+        logits[:, 3] -= 50.0                                 # one empty expert
+    ref_idx, _ = O.route(logits.numpy(), k)
+    idx = torch.from_numpy(ref_idx).cuda()
+    counts, offsets, sorted_f, row_of = moe.dispatch(idx, E)
+    rc, ro, rs, rr = O.dispatch(ref_idx, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(sorted_f.cpu().numpy(), rs)
+    assert np.array_equal(row_of.cpu().numpy(), rr)
+
+
+def test_dispatch_empty(moe):
+    counts, offsets, sorted_f, row_of = moe.dispatch(torch.empty(0, 2, dtype=torch.int32,
+                                                                 device="cuda"), 5)
+    assert counts.cpu().tolist() == [0] * 5 and offsets.cpu().tolist() == [0] * 6
+
+
+def test_dispatch_out_of_range_index_is_reported(moe):
+    idx = torch.tensor([[0, 1], [7, 2]], dtype=torch.int32, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        moe.dispatch(idx, 4)
+    assert ei.value.status == 1
+
+
+# ----------------------------------------------------------------- forward
+def _forward_case(moe, shape, seed=0, logit_bias=None, device_inputs=None):
+    d = make_inputs(shape, seed=seed, device="cpu") if device_inputs is None else device_inputs
+    logits = d["logits"]
+    if logit_bias is not None:
+        logits = logits + logit_bias
+    idx, w = O.route(logits.numpy(), shape.k)
+    dev = {n: d[n].cuda() for n in ("hidden", "w_gate_up", "w_down")}
+    out = moe.experts_forward(dev["hidden"], torch.from_numpy(idx).cuda(),
+                              torch.from_numpy(w.astype(np.float32)).cuda(),
+                              dev["w_gate_up"], dev["w_down"])
+    moe.workspace_status(moe.default_workspace())
+    ref = O.forward(d["hidden"].float().numpy(), idx, w.astype(np.float32),
+                    d["w_gate_up"].float().numpy(), d["w_down"].float().numpy())
+    return _to_np(out), ref
+
+
+@pytest.mark.parametrize("shape", [
+    shape_for("tiny"),
+    MoEShape(T=300, H=256, I=384, E=6, k=3),        # ragged m-tiles, several n-tiles
+    MoEShape(T=129, H=384, I=128, E=4, k=2),        # down GEMM with 128-wide n-tiles
+    MoEShape(T=1, H=512, I=256, E=16, k=4),         # a single token
+    MoEShape(T=40, H=1024, I=512, E=64, k=6),       # most experts get 1-10 rows
+    MoEShape(T=520, H=2048, I=1408, E=60, k=4),     # the Qwen-shaped layer, fewer tokens
+])
+def test_forward_bf16_parity(moe, shape):
+    out, ref = _forward_case(moe, shape)
+    err = O.rel_max_err(out, ref)
+    assert err <= BF16_TOL, err
+    assert np.all(np.isfinite(out))
+
+
+def test_forward_bf16_one_expert_takes_all(moe):
+    shape = MoEShape(T=700, H=256, I=256, E=8, k=2)
+    bias = torch.zeros(8)
+    bias[5] = 30.0                                  # every token routes to expert 5
+    out, ref = _forward_case(moe, shape, logit_bias=bias)
+    assert O.rel_max_err(out, ref) <= BF16_TOL
+
+
+def test_forward_bf16_zero_tokens(moe):
+    h = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    out = moe.experts_forward(h, torch.empty(0, 2, dtype=torch.int32, device="cuda"),
+                              torch.empty(0, 2, device="cuda"),
+                              torch.zeros(4, 256, 128, dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros(4, 128, 128, dtype=torch.bfloat16, device="cuda"))
+    assert out.shape == (0, 128)
+
+
+def test_forward_bf16_repeatable_and_token_order_equivariant(moe):
+    shape = MoEShape(T=256, H=256, I=256, E=8, k=2)
+    d = make_inputs(shape, seed=3)
+    idx, w = O.route(d["logits"].numpy(), 2)
+    args = [torch.from_numpy(idx).cuda(), torch.from_numpy(w.astype(np.float32)).cuda(),
+            d["w_gate_up"].cuda(), d["w_down"].cuda()]
+    h = d["hidden"].cuda()
+    a = moe.experts_forward(h, *args).float()
+    perm = torch.randperm(256, generator=torch.Generator().manual_seed(1))
+    b = moe.experts_forward(h[perm.cuda()].contiguous(), args[0][perm.cuda()].contiguous(),
+                            args[1][perm.cuda()].contiguous(), args[2], args[3]).float()
+    ref = a[perm.cuda()]
+    # fp32 atomics may add the k terms in another order: tiny differences only
+    assert (b - ref).abs().max().item() <= 1e-2 * ref.pow(2).mean().sqrt().item()
+
+
+@pytest.mark.parametrize("name,T,ntok", [("qwen", 4096, 48), ("dsv3", 8192, 4)])
+def test_forward_bf16_full_size_sampled(moe, name, T, ntok):
+    """Full workload size on the GPU; the oracle recomputes a sample of tokens
+    (each token's output depends only on its own row and its experts)."""
+    shape = shape_for(name, T)
+    d = make_inputs(shape, seed=0, device="cuda")
+    idx, w = moe.route(d["logits"], shape.k)
+    out = moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"])
+    moe.workspace_status(moe.default_workspace())
+    ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(T, ntok, replace=False))
+    sub_idx = ref_idx[toks]
+    experts = np.unique(sub_idx)
+    # oracle on the sampled tokens with only their experts, renumbered
+    remap = {int(e): i for i, e in enumerate(experts)}
+    loc_idx = np.vectorize(remap.get)(sub_idx).astype(np.int32)
+    ex_t = torch.from_numpy(experts).long().cuda()
+    wgu = d["w_gate_up"].index_select(0, ex_t).float().cpu().numpy()
+    wd = d["w_down"].index_select(0, ex_t).float().cpu().numpy()
+    hid = d["hidden"][torch.from_numpy(toks).cuda()].float().cpu().numpy()
+    ref = O.forward(hid, loc_idx, w.cpu().numpy()[toks], wgu, wd, dtype=np.float32)
+    got = out[torch.from_numpy(toks).cuda()].float().cpu().numpy()
+    assert O.rel_max_err(got, ref) <= BF16_TOL
+
+
+# ----------------------------------------------------------------- error paths
+def test_forward_rejects_unsupported(moe):
+    h = torch.zeros(4, 100, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        moe.experts_forward(h, torch.zeros(4, 2, dtype=torch.int32, device="cuda"),
+                            torch.zeros(4, 2, device="cuda"),
+                            torch.zeros(4, 256, 100, dtype=torch.bfloat16, device="cuda"),
+                            torch.zeros(4, 100, 128, dtype=torch.bfloat16, device="cuda"))
+    assert ei.value.status == 2
+
+
+def test_forward_bad_expert_index_reported(moe):
+    shape = MoEShape(T=16, H=128, I=128, E=4, k=2)
+    d = make_inputs(shape, seed=1, device="cuda")
+    idx = torch.zeros(16, 2, dtype=torch.int32, device="cuda")
+    idx[:, 1] = 1
+    idx[5, 1] = 9
+    ws = moe.Workspace("cuda")
+    moe.experts_forward(d["hidden"], idx, torch.full((16, 2), 0.5, device="cuda"),
+                        d["w_gate_up"], d["w_down"], workspace=ws)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.workspace_status(ws)
+    assert ei.value.status == 1
+    moe.workspace_status(ws)          # cleared
+
+
+def test_device_wait_timeout_is_reported_not_hung(moe):
+    st = moe.selftest_wait_timeout(limit_us=5000)
+    assert st == 4
+    # the context is still usable
+    x = torch.ones(10, device="cuda")
+    assert float(x.sum()) == 10.0
