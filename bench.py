@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Benchmark of the routed top-k MoE experts forward on GB300.
+
+One step = one pass of the whole path over one synthetic batch: router top-k
+(moe_route), then the experts forward (dispatch, grouped gate/up GEMM with
+SwiGLU, grouped down GEMM with the weighted combine, bf16 output).  Weights
+and inputs are resident in HBM when the timed region starts (``value``);
+``e2e`` repeats the measurement through host buffers with the copies inside
+the timed region.
+
+Default workload: the Qwen1.5-MoE-A2.7B-shaped layer in prefill (T=4096,
+H=2048, I=1408, E=60, k=4), bf16.  ``--workload`` selects another one.
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+path has no exchange step); ``value`` is the tokens of all ranks divided by
+the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (the plain eager expert loop) on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE experts fwd tokens/s, TFLOP/s or HBM GB/s as fraction of 1-GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# name -> (shape name, T, weight format, scale format)
+WORKLOADS = {
+    "qwen-prefill": ("qwen", 4096, "bf16", None),
+    "tiny": ("tiny", 64, "bf16", None),
+    "qwen-decode-1": ("qwen", 1, "bf16", None),
+    "qwen-decode-8": ("qwen", 8, "bf16", None),
+    "qwen-decode-32": ("qwen", 32, "bf16", None),
+    "qwen-decode-128": ("qwen", 128, "bf16", None),
+    "dsv3-prefill": ("dsv3", 8192, "bf16", None),
+    "dsv3-fp8-64-f32": ("dsv3_fp8", 64, "fp8", "f32"),
+    "dsv3-fp8-64-ue8m0": ("dsv3_fp8", 64, "fp8", "ue8m0"),
+    "dsv3-fp8-16384-f32": ("dsv3_fp8", 16384, "fp8", "f32"),
+    "dsv3-fp8-16384-ue8m0": ("dsv3_fp8", 16384, "fp8", "ue8m0"),
+}
+DESCRIPTIONS = {
+    "qwen": "Qwen1.5-MoE-A2.7B-shaped MoE layer",
+    "tiny": "tiny MoE FFN",
+    "dsv3": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) expert skew",
+    "dsv3_fp8": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) skew, e4m3 128x128 block-scaled weights",
+}
+L2_BYTES = 129 * 2 ** 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.isfile(p):
+        try:
+            d = json.load(open(p))
+            return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML every few ms."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+    def __init__(self, cuda_index: int):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            busid = self._bus_id(cuda_index)
+            if busid is None or nv.nvmlDeviceGetHandleByPciBusId_v2(busid, ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    @staticmethod
+    def _bus_id(i):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(i)
+            return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+        except Exception:
+            return None
+
+    def _loop(self):
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self._reason_fn(self.h, ctypes.byref(r)) == 0:
+                for bit, name in self.REASONS.items():
+                    if r.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "nvml"}
+
+
+# ------------------------------------------------------------------ workload
+def build_workload(name, device):
+    import torch
+    import mixture_experts_routed_top_gb300 as moe
+    from workloads import make_inputs, shape_for
+    sname, T, wfmt, sfmt = WORKLOADS[name]
+    shape = shape_for(sname, T)
+    d = make_inputs(shape, seed=0, device=device)
+    w = {"shape": shape, "wfmt": wfmt, "sfmt": sfmt, "logits": d["logits"],
+         "hidden": d["hidden"], "w_gate_up": d["w_gate_up"], "w_down": d["w_down"]}
+    if wfmt == "fp8":
+        w["q_gate_up"], w["s_gate_up"] = moe.quantize_fp8_blocks(d["w_gate_up"], sfmt)
+        w["q_down"], w["s_down"] = moe.quantize_fp8_blocks(d["w_down"], sfmt)
+        torch.cuda.synchronize()
+    return w
+
+
+def weights_of(w):
+    if w["wfmt"] == "fp8":
+        return dict(w_gate_up=w["q_gate_up"], w_down=w["q_down"], scale_gate_up=w["s_gate_up"],
+                    scale_down=w["s_down"], scale_fmt=w["sfmt"])
+    return dict(w_gate_up=w["w_gate_up"], w_down=w["w_down"])
+
+
+def algorithmic(w, counts):
+    """Algorithmic flops and bytes of one step (routed rows only; weight bytes
+    of the experts that received rows; hidden in, logits in, output out)."""
+    s = w["shape"]
+    rows = s.T * s.k
+    flops = 6.0 * s.H * s.I * rows
+    bpw = 1.0 if w["wfmt"] == "fp8" else 2.0
+    touched = int((counts > 0).sum())
+    scale_b = 0
+    if w["wfmt"] == "fp8":
+        per = 4 if w["sfmt"] == "f32" else 1
+        scale_b = (2 * s.I // 128) * (s.H // 128) * per + (s.H // 128) * (s.I // 128) * per
+    wbytes = touched * (3.0 * s.H * s.I * bpw + scale_b)
+    io = s.T * s.H * 2 * 2 + s.T * s.E * 4
+    return flops, wbytes, io, touched
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.isfile(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(kernel_key)
+        if not ent:
+            return None
+        src = os.path.join(ROOT, ent["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["bytes_per_launch"] if h == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env else os.cpu_count()
+
+
+class OracleSample:
+    """The CPU oracle (route + eager expert loop in float64) on the first n
+    tokens of the workload, with only the experts those tokens select copied
+    to the host (at most max_experts of them)."""
+
+    def __init__(self, w, n, max_experts=32):
+        import numpy as np
+        import torch
+        import oracle as O
+        self.O, self.w = O, w
+        s = w["shape"]
+        logits = w["logits"].float().cpu().numpy()
+        idx_all, _ = O.route(logits, s.k)
+        toks, ex = [], set()
+        for t in range(s.T):
+            new = ex | set(int(e) for e in idx_all[t])
+            if toks and (len(new) > max_experts or len(toks) >= n):
+                break
+            toks.append(t)
+            ex = new
+        toks, ex = np.array(toks), sorted(ex)
+        et = torch.tensor(ex, device=w["hidden"].device)
+        if w["wfmt"] == "fp8":
+            self.parts = [w["q_gate_up"].index_select(0, et).cpu().numpy(),
+                          w["s_gate_up"].index_select(0, et).cpu().numpy(),
+                          w["q_down"].index_select(0, et).cpu().numpy(),
+                          w["s_down"].index_select(0, et).cpu().numpy()]
+        else:
+            self.parts = [w["w_gate_up"].index_select(0, et).float().cpu().numpy(),
+                          w["w_down"].index_select(0, et).float().cpu().numpy()]
+        self.hid = w["hidden"][torch.from_numpy(toks).to(w["hidden"].device)].float().cpu().numpy()
+        self.logits = logits[toks]
+        self.remap = np.full(s.E, -1, np.int64)
+        self.remap[np.array(ex)] = np.arange(len(ex))
+        self.n = len(toks)
+        self.k = s.k
+
+    def run(self) -> float:
+        O = self.O
+        t0 = time.perf_counter()
+        idx, wt = O.route(self.logits, self.k)
+        lidx = self.remap[idx].astype("int32")
+        if self.w["wfmt"] == "fp8":
+            O.forward_fp8(self.hid, lidx, wt, *self.parts, self.w["sfmt"])
+        else:
+            O.forward(self.hid, lidx, wt, *self.parts)
+        return time.perf_counter() - t0
+
+
+def calibrated_oracle_sample(w, budget_s):
+    """Grow the token sample until one oracle run takes about budget_s."""
+    s = w["shape"]
+    n = 16
+    smp = OracleSample(w, n)
+    dt = smp.run()
+    while dt < budget_s / 2 and smp.n < s.T:
+        want = int(min(s.T, max(2 * smp.n, smp.n * budget_s / max(dt, 1e-3) * 0.8)))
+        nxt = OracleSample(w, want)
+        if nxt.n <= smp.n:
+            break
+        smp = nxt
+        dt = smp.run()
+    return smp, dt
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import mixture_experts_routed_top_gb300 as moe
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    moe.lib(build_if_missing=True)
+    w = build_workload(args.workload, dev)
+    s = w["shape"]
+    W = weights_of(w)
+    ws = moe.Workspace(dev)
+    out = torch.empty(s.T, s.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(logits, hidden):
+        idx, wt = moe.route(logits, s.k)
+        moe.experts_forward(hidden, idx, wt, out=out, workspace=ws, **W)
+        return idx
+
+    # routing statistics of the workload (outside any timed region)
+    idx = step(w["logits"], w["hidden"])
+    torch.cuda.synchronize()
+    moe.workspace_status(ws)
+    counts = torch.bincount(idx.flatten().long(), minlength=s.E).cpu().numpy()
+    flops, wbytes, io_bytes, touched = algorithmic(w, counts)
+    ws_bytes = moe.workspace_size(s.T, s.H, s.I, s.E, s.k, 1 if w["wfmt"] == "fp8" else 0)
+    working_set = wbytes + io_bytes
+    flush = working_set < 2 * L2_BYTES
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
+
+    for _ in range(args.warmup):
+        if flush:
+            flush_buf.zero_()
+        step(w["logits"], w["hidden"])
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = moe.launch_count()
+    moe.profile_begin()
+    with ClockSampler(dev.index) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
+            starts[i].record(stream)
+            step(w["logits"], w["hidden"])
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    stages = moe.profile_end()
+    launches = moe.launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    moe.workspace_status(ws)
+
+    # ---------------------------------------------------------- end to end
+    h_host = w["hidden"].cpu().pin_memory()
+    l_host = w["logits"].cpu().pin_memory()
+    o_host = torch.empty(s.T, s.H, dtype=torch.bfloat16).pin_memory()
+    h_dev = torch.empty_like(w["hidden"])
+    l_dev = torch.empty_like(w["logits"])
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        l_dev.copy_(l_host, non_blocking=True)
+        step(l_dev, h_dev)
+        o_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(2, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if not torch.equal(o_host, out.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
+
+    # ---------------------------------------------------------- report
+    peaks, peak_src = load_peaks()
+    ms_per_step = total_ms / args.steps
+    tok_s = world * s.T * args.steps / (total_ms / 1e3)
+    g1_ms, g1_n = stages["gemm1"]
+    g2_ms, g2_n = stages["gemm2"]
+    bytes_per_w = 1.0 if w["wfmt"] == "fp8" else 2.0
+    dominant = "gemm1" if g1_ms >= g2_ms else "gemm2"
+    d_ms, d_n = stages[dominant]
+    d_avg_s = d_ms / max(d_n, 1) / 1e3
+    share = (2.0 / 3.0) if dominant == "gemm1" else (1.0 / 3.0)
+    kern_flops = flops * share
+    kern_wbytes = wbytes * share
+    hbm_bound = s.T <= 256           # decode-sized batches stream weights
+    if hbm_bound:
+        achieved = kern_wbytes / d_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        pk = peaks["bf16_tflops"] * (2.0 if w["wfmt"] == "fp8" else 1.0)
+        achieved = kern_flops / d_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
+                "unit": "TFLOP/s", "frac": round(achieved / pk, 4)}
+    kernel_key = f"{dominant}:{args.workload}"
+    roof.update({"traffic": traffic_for(kernel_key), "kernel": dominant,
+                 "peak_source": f"{peak_src} ({'bf16 burst' if w['wfmt'] == 'bf16' else 'bf16 burst x2 nominal fp8/bf16 ratio'})",
+                 "algorithmic_per_launch": {"flops": kern_flops, "weight_bytes": kern_wbytes},
+                 "avg_launch_ms": round(d_avg_s * 1e3, 4)})
+    e2e_tok_s = world * s.T * args.steps / (e2e_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3" if w["wfmt"] == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "description": DESCRIPTIONS[WORKLOADS[args.workload][0]],
+                   "T": s.T, "H": s.H, "I": s.I, "E": s.E, "k": s.k,
+                   "scale_fmt": w["sfmt"], "parallelism": f"replicas x{world}",
+                   "l2": ("flushed before every timed step (512 MB write)" if flush else
+                          f"inputs larger than L2 ({working_set / 1e9:.2f} GB touched per step)"),
+                   "experts_touched": touched, "max_expert_rows": int(counts.max()),
+                   "workspace_bytes": ws_bytes},
+        "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
+        "weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
+        "roofline": roof,
+        "stages_ms_per_step": {k: round(v[0] / max(v[1], 1), 5) for k, v in stages.items()},
+        "e2e": {"value": round(e2e_tok_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_host.numel() * 2 + l_host.numel() * 4),
+                "d2h_bytes_per_step": int(o_host.numel() * 2)},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    return line, w
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen-prefill", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line, w = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp, _ = calibrated_oracle_sample(w, budget_s=8.0)
+        dt = smp.run()
+        line["cpu_baseline"] = {"value": round(smp.n / dt, 2), "unit": "tokens/s",
+                                "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"first {smp.n} tokens of the workload (route + "
+                                          f"float64 eager expert loop), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, timed on the host cores;
+    each step is the same bounded sample of the workload."""
+    import torch
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if WORKLOADS[args.workload][2] == "fp8" and dev.type != "cuda":
+        print(json.dumps({"impl": "reference",
+                          "unavailable": "the fp8 workload builds its weights with the GPU quantiser"}))
+        return 0
+    w = build_workload(args.workload, dev)
+    s = w["shape"]
+    smp, _ = calibrated_oracle_sample(w, budget_s=2.0)
+    for _ in range(args.warmup):
+        smp.run()
+    total = sum(smp.run() for _ in range(args.steps))
+    value = smp.n * args.steps / total
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": args.workload, "T": s.T, "H": s.H, "I": s.I, "E": s.E,
+                       "k": s.k},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"each step: first {smp.n} tokens of the workload "
+                                       f"(route + float64 eager expert loop)"},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

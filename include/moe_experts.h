@@ -184,6 +184,12 @@ moe_status moe_profile_begin(void);
 int moe_profile_end(float* stage_ms, int* stage_launches, int n);
 
 /*
+ * moe_launch_count - number of kernels this library has launched in this
+ * process (all entry points, all devices).  Driver memsets are not counted.
+ */
+long long moe_launch_count(void);
+
+/*
  * moe_selftest_wait_timeout - launch one kernel that waits on a device
  * barrier nothing will ever complete, with a wait limit of `limit_us`
  * microseconds; the kernel gives up, records MOE_ERR_TIMEOUT in the error

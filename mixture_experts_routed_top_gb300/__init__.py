@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
     "experts_forward", "quantize_fp8_blocks", "workspace_status", "set_decode_rows",
-    "get_decode_rows", "profile_begin", "profile_end", "selftest_wait_timeout",
+    "get_decode_rows", "profile_begin", "profile_end", "selftest_wait_timeout", "launch_count",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0",
 ]
@@ -57,6 +57,7 @@ _SIGS = {
     "moe_profile_begin": ([], _I),
     "moe_profile_end": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
     "moe_selftest_wait_timeout": ([_P, _SZ, _I, _P], _I),
+    "moe_launch_count": ([], ctypes.c_longlong),
 }
 
 
@@ -255,6 +256,11 @@ def profile_end():
     cnt = (ctypes.c_int * n)()
     lib().moe_profile_end(ms, cnt, n)
     return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().moe_launch_count())
 
 
 def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> int:

@@ -328,6 +328,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
   kern<<<a.num_sms, kThreads, L::SMEM, s>>>(*a.tm_a, *a.tm_b, p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include <cstdarg>
 #include <cstdio>
@@ -16,6 +17,11 @@
 #include "moe_internal.h"
 
 using namespace moe;
+
+namespace moe {
+static std::atomic<long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace moe
 
 namespace {
 
@@ -170,6 +176,8 @@ struct StageScope {
 extern "C" {
 
 int moe_version(void) { return 100; }
+
+long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 

@@ -42,6 +42,9 @@ struct DispatchBufs {
   int* touched;      // [E+1]: touched[0] = n, then expert ids ascending
 };
 
+// Counts every kernel launch the library makes (exported as moe_launch_count).
+void count_launches(int n);
+
 inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); }
 
 // Kernel launchers (return cudaGetLastError()).

@@ -84,6 +84,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
   else if (npl <= 8) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
   else if (npl <= 16) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
   else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -217,6 +218,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
     dispatch_place_kernel<<<nchunks, 32, 0, s>>>(topk_idx, n, E, d.blk_counts, d.sorted_f,
                                                  d.row_of);
   }
+  count_launches(nchunks ? 3 : 1);
   return cudaGetLastError();
 }
 
@@ -242,6 +244,7 @@ cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sort
   gather_bf16_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4*>(hidden), H / 8, k,
                                                        sorted_f, nvalid, rows,
                                                        static_cast<uint4*>(x_perm));
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -317,6 +320,7 @@ cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorte
   gather_fp8_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint2*>(hidden), H, k,
                                                       sorted_f, nvalid, rows, ue8m0,
                                                       reinterpret_cast<uint32_t*>(xq), xs);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -337,6 +341,7 @@ cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s) 
   const int grid = static_cast<int>(want < 152L * 16 ? want : 152L * 16);
   to_bf16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
                                       reinterpret_cast<uint2*>(dst), n4);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -394,6 +399,7 @@ cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, 
   if (nblk == 0) return cudaSuccess;
   quantize_blocks_kernel<<<static_cast<unsigned>(nblk), 256, 0, s>>>(
       static_cast<const uint4*>(w), rows, cols, ue8m0, reinterpret_cast<uint2*>(q), scale);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -412,6 +418,7 @@ __global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
 
 cudaError_t launch_selftest_wait(int* err, int limit_us, cudaStream_t s) {
   selftest_wait_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+  count_launches(1);
   return cudaGetLastError();
 }
 
