@@ -184,6 +184,37 @@ moe_status moe_profile_begin(void);
 int moe_profile_end(float* stage_ms, int* stage_launches, int n);
 
 /*
+ * moe_dispatch_noalloc - moe_dispatch for callers that cannot allocate
+ * device memory.  The page has no counterpart to this entry point; it exists
+ * for integration only.
+ *
+ * Some callers cannot provide a workspace: serving runtimes that reserve all
+ * device memory at start-up and forbid later cudaMalloc calls (which can fail
+ * mid-request and synchronise the device), or plugin hooks that must not
+ * allocate.  This variant keeps its scratch in a fixed device array inside
+ * the library (MOE_DISPATCH_NOALLOC_SCRATCH_BYTES, held on every GPU that
+ * loads the library until the process exits) and allocates nothing.  The
+ * caller still passes the inputs and the four outputs, with the same meaning
+ * and layout as moe_dispatch.
+ *   - Sizes whose moe_dispatch_workspace_size(T, E, k) exceeds the fixed
+ *     scratch are rejected with MOE_ERR_UNSUPPORTED before anything is
+ *     launched; moe_dispatch with a caller workspace has no such limit.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     each call clears the error word and rewrites the rest.  Calls that
+ *     overlap on the GPU (other streams, unordered host threads) race and
+ *     give wrong results.
+ *   - Out-of-range expert indices are skipped; the caller sees them as
+ *     offsets[E] < T*k.
+ */
+#define MOE_DISPATCH_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_dispatch_noalloc(const int32_t* topk_idx, int T, int E, int k,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_f,
+                                int32_t* row_of, void* stream);
+
+/*
  * moe_launch_count - number of kernels this library has launched in this
  * process (all entry points, all devices).  Driver memsets are not counted.
  */

@@ -37,6 +37,20 @@ moe_status fail(moe_status st, const char* fmt, ...) {
   return st;
 }
 
+}  // namespace
+
+moe_status moe::set_last_error(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+namespace {
+
 moe_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }

@@ -42,6 +42,9 @@ struct DispatchBufs {
   int* touched;      // [E+1]: touched[0] = n, then expert ids ascending
 };
 
+// Records the message moe_last_error() returns on this host thread; returns st.
+moe_status set_last_error(moe_status st, const char* fmt, ...);
+
 // Counts every kernel launch the library makes (exported as moe_launch_count).
 void count_launches(int n);
 
