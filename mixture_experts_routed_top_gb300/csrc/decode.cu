@@ -1,0 +1,294 @@
+// Small-token decode path: with few routed rows per expert the forward is a
+// stream over the touched experts' weights, so it runs on CUDA cores as
+// GEMVs that read every touched weight row exactly once (the page's
+// "Decode-stage switching" idea: a separate strategy for low token counts).
+//
+//   dispatch_small   one CTA: counts, scan, touched list, stable placement
+//   decode_gate_up   item = (touched expert, 4 features); warp = feature f:
+//                    gate and up rows of W_gate_up[e] streamed once, dotted
+//                    with the expert's token rows, h = silu(g) * u (bf16)
+//   decode_down      item = (touched expert, 4 output columns); warp = one
+//                    row of W_down[e]; Y[r, c] = topk_w * (h[r] . W_down[e,c])
+//   decode_combine   out[t] = sum_j Y[row_of[t*k+j]] in fp32 -> bf16
+// Work items are spread over a persistent grid (grid-stride), so every SM
+// streams weights whatever the number of touched experts.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------ dispatch
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+    const int32_t* __restrict__ idx, int n, int E, int* counts, int* offsets, int* tile_pref,
+    int* touched, int* sorted_f, int* row_of, int* err) {
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_cur[kMaxE];
+  __shared__ int s_warp[33];
+  const int tid = threadIdx.x;
+  if (tid < E) s_cnt[tid] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int f = tid; f < n; f += 1024) {
+    const int e = __ldg(idx + f);
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(err, ERR_BAD_INDEX);
+  __syncthreads();
+  const int c = tid < E ? s_cnt[tid] : 0;
+  const int tiles = (c + kBM - 1) / kBM;
+  const int tch = c > 0 ? 1 : 0;
+  int tot_c, tot_t, tot_h;
+  const int ex_c = block_exclusive_scan(c, s_warp, &tot_c);
+  const int ex_t = block_exclusive_scan(tiles, s_warp, &tot_t);
+  const int ex_h = block_exclusive_scan(tch, s_warp, &tot_h);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = ex_c;
+    tile_pref[tid] = ex_t;
+    if (tch) touched[1 + ex_h] = tid;
+    s_cur[tid] = ex_c;
+  }
+  if (tid == 0) {
+    offsets[E] = tot_c;
+    tile_pref[E] = tot_t;
+    touched[0] = tot_h;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int f0 = 0; f0 < n; f0 += 32) {
+      const int f = f0 + lane;
+      int e = (f < n) ? __ldg(idx + f) : -1;
+      if (e >= E) e = -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      int pos = -1;
+      if (e >= 0) {
+        pos = s_cur[e] + __popc(peers & lt);
+        sorted_f[pos] = f;
+      }
+      if (f < n) row_of[f] = pos;
+      __syncwarp();
+      if (e >= 0 && (peers & lt) == 0) s_cur[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// ------------------------------------------------------------ helpers
+// Weights are read once: bypass L1.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8], float acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// ------------------------------------------------------------ gate/up
+template <int MT>
+__global__ void __launch_bounds__(128) decode_gate_up_kernel(
+    const __nv_bfloat16* __restrict__ hidden, int H, int I, int k,
+    const __nv_bfloat16* __restrict__ wgu, const int* __restrict__ offsets,
+    const int* __restrict__ touched, const int* __restrict__ sorted_f,
+    __nv_bfloat16* __restrict__ h_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_e = I / 4;
+  const long n_items = static_cast<long>(__ldg(touched)) * per_e;
+  const int H8 = H / 8;
+  for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int e = __ldg(touched + 1 + static_cast<int>(item / per_e));
+    const int f = static_cast<int>(item % per_e) * 4 + warp;
+    const int r0 = __ldg(offsets + e);
+    const int m = __ldg(offsets + e + 1) - r0;
+    const uint4* wg = reinterpret_cast<const uint4*>(wgu + (static_cast<long>(e) * 2 * I + f) * H);
+    const uint4* wu = reinterpret_cast<const uint4*>(wgu + (static_cast<long>(e) * 2 * I + I + f) * H);
+    for (int t0 = 0; t0 < m; t0 += MT) {
+      const uint4* xr[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int tt = min(t0 + t, m - 1);
+        xr[t] = reinterpret_cast<const uint4*>(hidden) +
+                static_cast<long>(__ldg(sorted_f + r0 + tt) / k) * H8;
+      }
+      float ag[MT], au[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) ag[t] = au[t] = 0.f;
+#pragma unroll 4
+      for (int c = lane; c < H8; c += 32) {
+        float gf[8], uf[8];
+        bf16x8_to_f32(ld_stream(wg + c), gf);
+        bf16x8_to_f32(ld_stream(wu + c), uf);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          float xf[8];
+          bf16x8_to_f32(__ldg(xr[t] + c), xf);
+          ag[t] = dot8(gf, xf, ag[t]);
+          au[t] = dot8(uf, xf, au[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const float g = warp_sum(ag[t]);
+        const float u = warp_sum(au[t]);
+        if (lane == 0 && t0 + t < m)
+          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(silu_f(g) * u);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ down
+template <int MT>
+__global__ void __launch_bounds__(128) decode_down_kernel(
+    const __nv_bfloat16* __restrict__ h, int H, int I, const __nv_bfloat16* __restrict__ wd,
+    const int* __restrict__ offsets, const int* __restrict__ touched,
+    const int* __restrict__ sorted_f, const float* __restrict__ topk_w, float* __restrict__ Y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_e = H / 4;
+  const long n_items = static_cast<long>(__ldg(touched)) * per_e;
+  const int I8 = I / 8;
+  for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int e = __ldg(touched + 1 + static_cast<int>(item / per_e));
+    const int c = static_cast<int>(item % per_e) * 4 + warp;
+    const int r0 = __ldg(offsets + e);
+    const int m = __ldg(offsets + e + 1) - r0;
+    const uint4* wr = reinterpret_cast<const uint4*>(wd + (static_cast<long>(e) * H + c) * I);
+    for (int t0 = 0; t0 < m; t0 += MT) {
+      const uint4* hr[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t)
+        hr[t] = reinterpret_cast<const uint4*>(h) + static_cast<long>(r0 + min(t0 + t, m - 1)) * I8;
+      float acc[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+#pragma unroll 4
+      for (int v = lane; v < I8; v += 32) {
+        float wf[8];
+        bf16x8_to_f32(ld_stream(wr + v), wf);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          float xf[8];
+          bf16x8_to_f32(__ldg(hr[t] + v), xf);
+          acc[t] = dot8(wf, xf, acc[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const float y = warp_sum(acc[t]);
+        if (lane == 0 && t0 + t < m) {
+          const int r = r0 + t0 + t;
+          Y[static_cast<long>(r) * H + c] = y * __ldg(topk_w + __ldg(sorted_f + r));
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ combine
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __restrict__ Y,
+                                                             const int* __restrict__ row_of,
+                                                             int T, int H, int k,
+                                                             uint2* __restrict__ out) {
+  const int H4 = H / 4;
+  const long total = static_cast<long>(T) * H4;
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long t = i / H4;
+    const int c4 = static_cast<int>(i - t * H4);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int r = __ldg(row_of + t * k + j);
+      if (r < 0) continue;
+      const float4 y = __ldg(Y + static_cast<long>(r) * H4 + c4);
+      s.x += y.x;
+      s.y += y.y;
+      s.z += y.z;
+      s.w += y.w;
+    }
+    out[i] = make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+  }
+}
+
+// ------------------------------------------------------------ launchers
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
+                                  const DispatchBufs& d, cudaStream_t s) {
+  const int n = T * k;
+  dispatch_small_kernel<<<1, 1024, 0, s>>>(topk_idx, n, E, d.counts, d.offsets, d.tile_pref,
+                                           d.touched, d.sorted_f, d.row_of, d.err);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+static int mt_for(int T) { return T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1; }
+
+static int decode_grid(const DecodeArgs& a, long items_per_expert) {
+  const long n_exp_max = a.E < static_cast<long>(a.T) * a.k ? a.E : static_cast<long>(a.T) * a.k;
+  const long items = n_exp_max * items_per_expert;
+  const long slots = static_cast<long>(a.num_sms) * 16;
+  return static_cast<int>(items < slots ? items : slots);
+}
+
+cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s) {
+  const int grid = decode_grid(a, a.I / 4);
+  auto* hb = static_cast<__nv_bfloat16*>(a.h);
+  auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
+  auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
+  switch (mt_for(a.T)) {
+    case 8: decode_gate_up_kernel<8><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 4: decode_gate_up_kernel<4><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 2: decode_gate_up_kernel<2><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    default: decode_gate_up_kernel<1><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s) {
+  const int grid = decode_grid(a, a.H / 4);
+  auto* hb = static_cast<const __nv_bfloat16*>(a.h);
+  auto* w = static_cast<const __nv_bfloat16*>(a.w_down);
+  switch (mt_for(a.T)) {
+    case 8: decode_down_kernel<8><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    case 4: decode_down_kernel<4><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    case 2: decode_down_kernel<2><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    default: decode_down_kernel<1><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
+  const long total = static_cast<long>(a.T) * (a.H / 4);
+  const long want = (total + 255) / 256;
+  const long slots = static_cast<long>(a.num_sms) * 16;
+  const int grid = static_cast<int>(want < slots ? want : slots);
+  decode_combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(a.Y), a.row_of, a.T,
+                                             a.H, a.k, static_cast<uint2*>(a.out));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

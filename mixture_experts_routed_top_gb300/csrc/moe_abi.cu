@@ -64,7 +64,7 @@ int g_decode_rows = -1;  // < 0: default
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
   size_t counts, offsets, tile_pref, touched, sorted_f, row_of, blk_counts;
-  size_t xa, xa_scale, hb, hb_scale, out32;
+  size_t xa, xa_scale, hb, hb_scale, out32, ydec;
   size_t total;
 };
 
@@ -91,6 +91,7 @@ WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
   L.hb = take(n * I * esz);
   L.hb_scale = take(fp8 ? n * (I / 128) * 4 : 0);
   L.out32 = take(T * H * 4);
+  L.ydec = take(n <= kDecodeRowsMax ? n * H * 4 : 0);
   L.total = align_up(off, 1024);
   return L;
 }
@@ -195,8 +196,10 @@ long long moe_launch_count(void) { return g_launches.load(std::memory_order_rela
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-void moe_set_decode_rows(int rows) { g_decode_rows = rows; }
-int moe_get_decode_rows(void) { return g_decode_rows < 0 ? 0 : g_decode_rows; }
+void moe_set_decode_rows(int rows) {
+  g_decode_rows = rows < 0 ? -1 : (rows > kDecodeRowsMax ? kDecodeRowsMax : rows);
+}
+int moe_get_decode_rows(void) { return g_decode_rows < 0 ? kDecodeRowsDefault : g_decode_rows; }
 
 moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                      void* stream) {
@@ -314,6 +317,48 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
   void* hb = w + L.hb;
   float* out32 = reinterpret_cast<float*>(w + L.out32);
 
+  const int sms = num_sms();
+  cudaError_t e;
+  if (!fp8 && n <= moe_get_decode_rows()) {
+    // small-token path: stream the touched experts' weights once
+    DecodeArgs a;
+    a.hidden = hidden;
+    a.w_gate_up = w_gate_up;
+    a.w_down = w_down;
+    a.topk_w = topk_w;
+    a.offsets = d.offsets;
+    a.touched = d.touched;
+    a.sorted_f = d.sorted_f;
+    a.row_of = d.row_of;
+    a.h = hb;
+    a.Y = reinterpret_cast<float*>(w + L.ydec);
+    a.out = out;
+    a.T = T;
+    a.H = H;
+    a.I = I;
+    a.E = E;
+    a.k = k;
+    a.num_sms = sms;
+    {
+      StageScope sc(s, MOE_STAGE_DISPATCH);
+      if ((e = launch_dispatch_small(topk_idx, T, E, k, d, s)) != cudaSuccess)
+        return cuda_fail(e, "dispatch_small");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM1);
+      if ((e = launch_decode_gate_up(a, s)) != cudaSuccess) return cuda_fail(e, "decode_gate_up");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM2);
+      if ((e = launch_decode_down(a, s)) != cudaSuccess) return cuda_fail(e, "decode_down");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_FINISH);
+      if ((e = launch_decode_combine(a, s)) != cudaSuccess) return cuda_fail(e, "decode_combine");
+    }
+    return MOE_OK;
+  }
+
   CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
   moe_status st;
   if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n)) != MOE_OK) return st;
@@ -325,7 +370,6 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
                      static_cast<uint64_t>(E) * H)) != MOE_OK)
     return st;
 
-  cudaError_t e;
   {
     StageScope sc(s, MOE_STAGE_DISPATCH);
     if ((e = launch_dispatch(topk_idx, T, E, k, d, s)) != cudaSuccess) return cuda_fail(e, "dispatch");
@@ -335,7 +379,6 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     if ((e = cudaMemsetAsync(out32, 0, static_cast<size_t>(T) * H * 4, s)) != cudaSuccess)
       return cuda_fail(e, "memset");
   }
-  const int sms = num_sms();
   GroupedGemmArgs g{};
   g.offsets = d.offsets;
   g.tile_pref = d.tile_pref;

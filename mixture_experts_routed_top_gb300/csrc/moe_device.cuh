@@ -196,4 +196,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Exclusive scan of one value per thread; blockDim.x must be 1024 and all
+// threads must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int ws = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws += y;
+    }
+    s_warp[lane] = ws - w;  // exclusive prefix of warp totals
+    if (lane == 31) s_warp[32] = ws;
+  }
+  __syncthreads();
+  const int res = s_warp[warp] + x - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return res;
+}
+
 }  // namespace moe

@@ -81,6 +81,29 @@ struct GroupedGemmArgs {
   const float* topk_w;
   int num_sms;
 };
+// Small-token decode path.
+struct DecodeArgs {
+  const void* hidden;        // bf16 [T, H]
+  const void* w_gate_up;     // bf16 [E, 2I, H]
+  const void* w_down;        // bf16 [E, H, I]
+  const float* topk_w;       // [T, k]
+  const int* offsets;        // [E+1]
+  const int* touched;        // [E+1]
+  const int* sorted_f;       // [T*k]
+  const int* row_of;         // [T*k]
+  void* h;                   // bf16 [T*k, I]
+  float* Y;                  // fp32 [T*k, H], weighted rows
+  void* out;                 // bf16 [T, H]
+  int T, H, I, E, k, num_sms;
+};
+constexpr int kDecodeRowsDefault = 16;    // T*k at or below: decode path (measured crossover)
+constexpr int kDecodeRowsMax = 2048;      // the decode path's workspace is sized up to this
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
+                                  const DispatchBufs& d, cudaStream_t s);
+cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
+
 cudaError_t launch_gemm1_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 

@@ -115,35 +115,6 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
     blk_counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
 }
 
-// Exclusive scan of one value per thread over a block of 1024 threads.
-__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_warp[lane];
-    int ws = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, ws, off);
-      if (lane >= off) ws += y;
-    }
-    s_warp[lane] = ws - w;  // exclusive prefix of warp totals
-    if (lane == 31) s_warp[32] = ws;
-  }
-  __syncthreads();
-  const int res = s_warp[warp] + x - v;
-  *total = s_warp[32];
-  __syncthreads();
-  return res;
-}
-
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks, int* blk_counts,
                                                              int* counts, int* offsets,
                                                              int* tile_pref, int* touched) {

@@ -92,6 +92,17 @@ def test_dispatch_out_of_range_index_is_reported(moe):
 
 
 # ----------------------------------------------------------------- forward
+PATHS = {"prefill": 0, "decode": 2048}
+
+
+@pytest.fixture
+def path(moe, request):
+    """Force the grouped tensor-core path or the decode path."""
+    moe.set_decode_rows(PATHS[request.param])
+    yield request.param
+    moe.set_decode_rows(-1)
+
+
 def _forward_case(moe, shape, seed=0, logit_bias=None, device_inputs=None):
     d = make_inputs(shape, seed=seed, device="cpu") if device_inputs is None else device_inputs
     logits = d["logits"]
@@ -108,27 +119,74 @@ def _forward_case(moe, shape, seed=0, logit_bias=None, device_inputs=None):
     return _to_np(out), ref
 
 
-@pytest.mark.parametrize("shape", [
+SMALL_SHAPES = [
     shape_for("tiny"),
     MoEShape(T=300, H=256, I=384, E=6, k=3),        # ragged m-tiles, several n-tiles
     MoEShape(T=129, H=384, I=128, E=4, k=2),        # down GEMM with 128-wide n-tiles
     MoEShape(T=1, H=512, I=256, E=16, k=4),         # a single token
     MoEShape(T=40, H=1024, I=512, E=64, k=6),       # most experts get 1-10 rows
-    MoEShape(T=520, H=2048, I=1408, E=60, k=4),     # the Qwen-shaped layer, fewer tokens
-])
-def test_forward_bf16_parity(moe, shape):
+    MoEShape(T=3, H=128, I=128, E=2, k=2),          # k = E
+]
+
+
+@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+def test_forward_bf16_parity(moe, shape, path):
     out, ref = _forward_case(moe, shape)
     err = O.rel_max_err(out, ref)
     assert err <= BF16_TOL, err
     assert np.all(np.isfinite(out))
 
 
-def test_forward_bf16_one_expert_takes_all(moe):
-    shape = MoEShape(T=700, H=256, I=256, E=8, k=2)
+@pytest.mark.parametrize("path", ["prefill"], indirect=True)
+def test_forward_bf16_parity_qwen_shape_520_tokens(moe, path):
+    out, ref = _forward_case(moe, MoEShape(T=520, H=2048, I=1408, E=60, k=4))
+    assert O.rel_max_err(out, ref) <= BF16_TOL
+
+
+@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+def test_forward_bf16_one_expert_takes_all(moe, path):
+    shape = MoEShape(T=700 if path == "prefill" else 90, H=256, I=256, E=8, k=2)
     bias = torch.zeros(8)
     bias[5] = 30.0                                  # every token routes to expert 5
     out, ref = _forward_case(moe, shape, logit_bias=bias)
     assert O.rel_max_err(out, ref) <= BF16_TOL
+
+
+def test_decode_and_prefill_paths_agree(moe):
+    shape = MoEShape(T=96, H=512, I=384, E=16, k=4)
+    d = make_inputs(shape, seed=5, device="cuda")
+    idx, w = moe.route(d["logits"], shape.k)
+    outs = []
+    for rows in (0, 2048):
+        moe.set_decode_rows(rows)
+        outs.append(moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"]).float())
+    moe.set_decode_rows(-1)
+    # different accumulation orders: a one-ulp bf16 flip at the largest
+    # outputs is ~1.7 % of rms, so the bound is the parity tolerance
+    ref = outs[0].pow(2).mean().sqrt().item()
+    assert (outs[0] - outs[1]).abs().max().item() <= BF16_TOL * ref
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128])
+def test_forward_bf16_decode_workloads_full(moe, T):
+    """The Qwen-shaped decode workloads at their full size, every token
+    checked against the oracle, through the default path choice."""
+    shape = shape_for("qwen", T)
+    d = make_inputs(shape, seed=0, device="cuda")
+    idx, w = moe.route(d["logits"], shape.k)
+    out = moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"])
+    moe.workspace_status(moe.default_workspace())
+    ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    experts = np.unique(ref_idx)
+    remap = np.full(shape.E, -1, np.int64)
+    remap[experts] = np.arange(len(experts))
+    ex_t = torch.from_numpy(experts).long().cuda()
+    ref = O.forward(d["hidden"].float().cpu().numpy(), remap[ref_idx].astype(np.int32),
+                    w.cpu().numpy(), d["w_gate_up"].index_select(0, ex_t).float().cpu().numpy(),
+                    d["w_down"].index_select(0, ex_t).float().cpu().numpy())
+    assert O.rel_max_err(out.float().cpu().numpy(), ref) <= BF16_TOL
 
 
 def test_forward_bf16_zero_tokens(moe):
@@ -194,7 +252,8 @@ def test_forward_rejects_unsupported(moe):
     assert ei.value.status == 2
 
 
-def test_forward_bad_expert_index_reported(moe):
+@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+def test_forward_bad_expert_index_reported(moe, path):
     shape = MoEShape(T=16, H=128, I=128, E=4, k=2)
     d = make_inputs(shape, seed=1, device="cuda")
     idx = torch.zeros(16, 2, dtype=torch.int32, device="cuda")
