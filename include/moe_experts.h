@@ -118,8 +118,9 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
  *               down(silu(gate x_t) * up x_t) of expert topk_idx[t,j],
  *               accumulated in fp32 and rounded once to bf16
  *   ws          device scratch, >= moe_workspace_size() bytes, 256-B aligned
- * Requirements: H % 128 == 0, I % 128 == 0, 1 <= k <= min(E, 32),
- * E <= 1024, T >= 0 (T = 0 is a no-op).  Other shapes: MOE_ERR_UNSUPPORTED.
+ * Requirements: H % 128 == 0 (H % 256 == 0 for FP8 weights), I % 128 == 0,
+ * 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 is a no-op).  Other
+ * shapes: MOE_ERR_UNSUPPORTED.
  * FP8 weights with MOE_SCALE_NONE: MOE_ERR_INVALID_ARG.
  * Inputs are never written; out is fully overwritten.
  * Calls that share one ws must be ordered (same stream or synchronised).

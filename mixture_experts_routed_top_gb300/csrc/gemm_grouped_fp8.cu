@@ -1,0 +1,453 @@
+// FP8 (e4m3) block-scaled grouped GEMMs of the routed experts forward.
+//
+// Weights carry one scale per 128x128 block, activations one per 1x128 block
+// along the contraction axis (float32, or UE8M0 powers of two).  A K-block
+// here is 128 e4m3 values = one 128-byte swizzled row = exactly one scale
+// block, so
+//     acc[r, c] = sum_kb s_a[r, kb] * s_w[c/128, kb] * (sum_{k in kb} qa[r,k] qw[c,k])
+// The tensor core computes each K-block's inner sum into a fresh TMEM buffer
+// (tcgen05.mma kind::f8f6f4, M=128, N=256, K=32 per instruction); two
+// epilogue warpgroups read it back and fold it into fp32 register
+// accumulators with the block's scale product.  Two 256-column TMEM buffers
+// let the MMA of K-block kb+1 run while K-block kb is being promoted.
+//
+// Roles (persistent, one CTA per SM, 320 threads):
+//   warp 0      TMA producer, 4-stage ring of A 128x128 B + B 256x128 B
+//   warp 1      TMEM allocator + MMA issuer
+//   warps 2-9   epilogue: warpgroup 0 = warps 2-5, warpgroup 1 = warps 6-9;
+//               thread = tile row (TMEM lane), warpgroup = half of the columns
+//     gate/up:  warpgroup g owns gate columns 64g..64g+63 and the matching up
+//               columns; at tile end h = silu(g)*u is re-quantised per row
+//               over the tile's 128 columns (one 1x128 block of I; the two
+//               warpgroups exchange their row maxima through shared memory)
+//     down:     warpgroup g owns output columns 128g..128g+127 (one weight
+//               block row); at tile end y * routing weight is added into the
+//               fp32 accumulator of the token (vector atomics)
+// All waits are bounded as in the bf16 kernel.
+#include <cuda_fp8.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // e4m3 per 128-byte row = one scale block
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kBufCols = 256;
+constexpr int kBoxBytes = 128 * 128;
+
+enum { EPI_SWIGLU_Q = 0, EPI_COMBINE = 1 };
+
+struct L8 {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES;
+  static constexpr int OFF_B = kStages * A_BYTES;
+  static constexpr int OFF_BAR = OFF_B + kStages * B_BYTES;
+  static constexpr int NBARS = 2 * kStages + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int OFF_AMAX = OFF_MISC + 16;              // float [2 tiles][2 wg][128]
+  static constexpr int OFF_OFF = OFF_AMAX + 4 * 128 * 4;
+  static constexpr int OFF_PREF = OFF_OFF + (kMaxE + 1) * 4;
+  static constexpr int BYTES = OFF_PREF + (kMaxE + 1) * 4;
+  static constexpr int SMEM = BYTES + 1024;
+};
+
+struct Fp8Dev {
+  const int* offsets;
+  const int* tile_pref;
+  int E, K, I, H, k, n_rows;
+  int* err;
+  const void* a_scale;  // [K/128, n_rows], fp32 or UE8M0 byte
+  const void* w_scale;  // [E, Nw/128, K/128], fp32 or UE8M0 byte
+  int ue8m0;
+  uint8_t* hq;          // gate/up: h codes [n_rows, I]
+  void* hs;             // gate/up: h scales [I/128, n_rows]
+  float* out32;         // down: [T, H]
+  const int* sorted_f;
+  const float* topk_w;
+};
+
+__device__ __forceinline__ void decode_tile8(int tile, int NT, int E, const int* s_pref, int& e,
+                                             int& m, int& n) {
+  const int v = tile / NT;
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pref[mid] <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  e = lo;
+  const int mt = s_pref[e + 1] - s_pref[e];
+  const int local = tile - s_pref[e] * NT;
+  n = local / mt;
+  m = local - n * mt;
+}
+
+__device__ __forceinline__ float load_scale(const void* base, long i, int ue8m0) {
+  if (ue8m0) {
+    const uint32_t b = __ldg(static_cast<const uint8_t*>(base) + i);
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+  }
+  return __ldg(static_cast<const float*>(base) + i);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a,
+                            const __grid_constant__ CUtensorMap tm_b, const Fp8Dev p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + L8::OFF_B;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L8::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* pfull = bars + 2 * kStages;
+  uint64_t* pempty = pfull + 2;
+  uint64_t* fin = pempty + 2;
+  uint64_t* amax_bar = fin + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L8::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L8::OFF_MISC + 4);
+  float* s_amax = reinterpret_cast<float*>(smem + L8::OFF_AMAX);
+  int* s_off = reinterpret_cast<int*>(smem + L8::OFF_OFF);
+  int* s_pref = reinterpret_cast<int*>(smem + L8::OFF_PREF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  for (int i = threadIdx.x; i <= E; i += kThreads) {
+    s_off[i] = p.offsets[i];
+    s_pref[i] = p.tile_pref[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&pfull[b]), 1);
+      mbar_init(smem_u32(&pempty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(fin), 1);
+    mbar_init(smem_u32(amax_bar), kEpiWarps * 32);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  const int NT = (EPI == EPI_SWIGLU_Q) ? p.I / 128 : p.H / BN;
+  const int total = s_pref[E] * NT;
+  const int KB = p.K / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t ph = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, m, n;
+        decode_tile8(tile, NT, E, s_pref, e, m, n);
+        const int arow = s_off[e] + m * BM;
+        const int brow = (EPI == EPI_SWIGLU_Q) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
+                                 ERR_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, L8::STAGE_TX);
+          const uint32_t a_dst = smem_u32(sA + stage * L8::A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + stage * L8::B_BYTES);
+          tma_load_2d(&tm_a, fb, a_dst, kb * BK, arow);
+          if (EPI == EPI_SWIGLU_Q) {
+            tma_load_2d(&tm_b, fb, b_dst, kb * BK, brow);
+            tma_load_2d(&tm_b, fb, b_dst + kBoxBytes, kb * BK, brow + p.I);
+          } else {
+            tma_load_2d(&tm_b, fb, b_dst, kb * BK, brow);
+            tma_load_2d(&tm_b, fb, b_dst + kBoxBytes, kb * BK, brow + 128);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (ph << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < kStages; ++s) {
+        if ((issued >> s) & 1u) {
+          volatile int no_abort = 0;
+          mbar_wait_bounded(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
+                            ERR_TIMEOUT_PRODUCER, 20000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t g = 0;  // K-blocks issued so far (selects the partial buffer)
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int b = g & 1;
+          const uint32_t bph = (g >> 1) & 1;
+          if (!mbar_wait_bounded(smem_u32(&pempty[b]), bph ^ 1u, s_abort, p.err, ERR_TIMEOUT_MMA) ||
+              !mbar_wait_bounded(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + b * kBufCols;
+          const uint64_t ad = sdesc_k_sw128(smem_u32(sA + stage * L8::A_BYTES));
+          const uint64_t bd = sdesc_k_sw128(smem_u32(sB + stage * L8::B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            umma_f8(d, ad + 2 * kk, bd + 2 * kk, idesc, kk != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&empty[stage]));
+          umma_commit(smem_u32(&pfull[b]));
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (g > 0) {
+        umma_commit(smem_u32(fin));
+        volatile int no_abort = 0;
+        mbar_wait_bounded(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - 2) >> 2;  // warpgroup 0 or 1
+    const int q = warp & 3;          // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const int KBn = p.K / 128;
+    uint32_t g = 0;
+    uint32_t amax_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      int e, m, n;
+      decode_tile8(tile, NT, E, s_pref, e, m, n);
+      const int m_e = s_off[e + 1] - s_off[e];
+      const bool valid = m * BM + r < m_e;
+      const long R = static_cast<long>(s_off[e]) + m * BM + r;
+      // weight block rows of this tile's columns
+      long wrow0, wrow1;
+      if (EPI == EPI_SWIGLU_Q) {
+        wrow0 = static_cast<long>(e) * (2 * p.I / 128) + n;              // gate block row
+        wrow1 = static_cast<long>(e) * (2 * p.I / 128) + p.I / 128 + n;  // up block row
+      } else {
+        wrow0 = static_cast<long>(e) * (p.H / 128) + 2 * n + wg;         // this warpgroup's block row
+        wrow1 = wrow0;
+      }
+      float acc0[64], acc1[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
+      for (int kb = 0; kb < KB; ++kb, ++g) {
+        const float sa = valid ? load_scale(p.a_scale, static_cast<long>(kb) * p.n_rows + R, p.ue8m0) : 0.f;
+        const float s0 = sa * load_scale(p.w_scale, wrow0 * KBn + kb, p.ue8m0);
+        const float s1 = sa * load_scale(p.w_scale, wrow1 * KBn + kb, p.ue8m0);
+        const int b = g & 1;
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = mbar_wait_bounded(smem_u32(&pfull[b]), (g >> 1) & 1, s_abort, p.err,
+                                   ERR_TIMEOUT_EPILOGUE);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t v[32];
+        if (EPI == EPI_SWIGLU_Q) {
+          // gate columns 64wg.., up columns 128+64wg..
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_32x32b_x32(tb + 64 * wg + 32 * h, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc0[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc0[32 * h + i]);
+            tmem_ld_32x32b_x32(tb + 128 + 64 * wg + 32 * h, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc1[32 * h + i] = fmaf(__uint_as_float(v[i]), s1, acc1[32 * h + i]);
+          }
+        } else {
+          // output columns 128wg .. 128wg+127 -> acc0[0..63], acc1[0..63]
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_32x32b_x32(tb + 128 * wg + 32 * h, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc0[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc0[32 * h + i]);
+            tmem_ld_32x32b_x32(tb + 128 * wg + 64 + 32 * h, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc1[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc1[32 * h + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
+      }
+      if (!ok) break;
+
+      if (EPI == EPI_SWIGLU_Q) {
+        // h = silu(g) * u over this warpgroup's 64 columns; the 1x128 block
+        // is the tile's 128 columns, shared with the other warpgroup.
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc0[i] = silu_f(acc0[i]) * acc1[i];
+          amax = fmaxf(amax, fabsf(acc0[i]));
+        }
+        float* am = s_amax + (amax_phase ? 256 : 0);   // double-buffered by tile
+        am[wg * 128 + r] = amax;
+        mbar_arrive(smem_u32(amax_bar));
+        int a_ok = 1;
+        if (lane == 0)
+          a_ok = mbar_wait_bounded(smem_u32(amax_bar), amax_phase, s_abort, p.err,
+                                   ERR_TIMEOUT_EPILOGUE);
+        a_ok = __shfl_sync(0xffffffffu, a_ok, 0);
+        if (!a_ok) {
+          ok = false;
+          break;
+        }
+        amax = fmaxf(am[r], am[128 + r]);
+        amax_phase ^= 1u;
+        // scale as in the weight quantiser: amax/448 or its power-of-two ceiling
+        float sc = 1.0f;
+        uint32_t stored = p.ue8m0 ? 127u : __float_as_uint(1.0f);
+        if (amax != 0.f) {
+          const float qv = amax / 448.0f;
+          if (!p.ue8m0) {
+            sc = qv;
+            stored = __float_as_uint(qv);
+          } else {
+            const uint32_t bits = __float_as_uint(qv);
+            int bexp = static_cast<int>((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) ? 1 : 0);
+            bexp = bexp > 254 ? 254 : bexp;
+            stored = static_cast<uint32_t>(bexp);
+            sc = bexp == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(stored << 23);
+          }
+        }
+        const float inv = 1.0f / sc;
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.hq + R * p.I + n * 128 + 64 * wg);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int i = 16 * j + 4 * t;
+              w4[t] = e4m3x4(acc0[i] * inv, acc0[i + 1] * inv, acc0[i + 2] * inv, acc0[i + 3] * inv);
+            }
+            dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          if (wg == 0) {
+            const long si = static_cast<long>(n) * p.n_rows + R;
+            if (p.ue8m0) static_cast<uint8_t*>(p.hs)[si] = static_cast<uint8_t>(stored);
+            else static_cast<uint32_t*>(p.hs)[si] = stored;
+          }
+        }
+      } else {
+        if (valid) {
+          const int f = __ldg(p.sorted_f + R);
+          const int tok = f / p.k;
+          const float wgt = __ldg(p.topk_w + f);
+          float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + 128 * wg;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            atomicAdd(reinterpret_cast<float4*>(orow + 4 * j),
+                      make_float4(wgt * acc0[4 * j], wgt * acc0[4 * j + 1], wgt * acc0[4 * j + 2],
+                                  wgt * acc0[4 * j + 3]));
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            atomicAdd(reinterpret_cast<float4*>(orow + 64 + 4 * j),
+                      make_float4(wgt * acc1[4 * j], wgt * acc1[4 * j + 1], wgt * acc1[4 * j + 2],
+                                  wgt * acc1[4 * j + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int EPI>
+cudaError_t launch_fp8_impl(const GroupedGemmFp8Args& a, cudaStream_t s) {
+  auto kern = grouped_gemm_fp8_kernel<EPI>;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static bool attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L8::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  Fp8Dev p;
+  p.offsets = a.offsets;
+  p.tile_pref = a.tile_pref;
+  p.E = a.E;
+  p.K = a.K;
+  p.I = a.I;
+  p.H = a.H;
+  p.k = a.k;
+  p.n_rows = a.n_rows;
+  p.err = a.err;
+  p.a_scale = a.a_scale;
+  p.w_scale = a.w_scale;
+  p.ue8m0 = a.ue8m0 ? 1 : 0;
+  p.hq = static_cast<uint8_t*>(a.hq);
+  p.hs = a.hs;
+  p.out32 = a.out32;
+  p.sorted_f = a.sorted_f;
+  p.topk_w = a.topk_w;
+  kern<<<a.num_sms, kThreads, L8::SMEM, s>>>(*a.tm_a, *a.tm_b, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s) {
+  return launch_fp8_impl<EPI_SWIGLU_Q>(a, s);
+}
+
+cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s) {
+  return launch_fp8_impl<EPI_COMBINE>(a, s);
+}
+
+}  // namespace moe

@@ -300,7 +300,10 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
   if (ws_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE, "moe_experts_forward: workspace %zu < %zu bytes", ws_bytes,
                 L.total);
-  if (fp8) return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: FP8 path not built yet");
+  if (fp8 && H % 256)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: FP8 weights need H % 256 == 0");
+  if (fp8 && (!aligned(scale_gate_up, 4) || !aligned(scale_down, 4)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: scale buffers must be 4-byte aligned");
 
   uint8_t* w = static_cast<uint8_t*>(ws);
   const long n = static_cast<long>(T) * k;
@@ -355,6 +358,77 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     {
       StageScope sc(s, MOE_STAGE_FINISH);
       if ((e = launch_decode_combine(a, s)) != cudaSuccess) return cuda_fail(e, "decode_combine");
+    }
+    return MOE_OK;
+  }
+
+  if (fp8) {
+    const bool ue = sfmt == MOE_SCALE_UE8M0;
+    uint8_t* xq = w + L.xa;
+    void* xs = w + L.xa_scale;
+    uint8_t* hq = w + L.hb;
+    void* hs = w + L.hb_scale;
+    float* out32 = reinterpret_cast<float*>(w + L.out32);
+    CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
+    moe_status st;
+    if ((st = make_map(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, n)) != MOE_OK) return st;
+    if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H,
+                       static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+      return st;
+    if ((st = make_map(&tm_h, hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, n)) != MOE_OK) return st;
+    if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I,
+                       static_cast<uint64_t>(E) * H)) != MOE_OK)
+      return st;
+    {
+      StageScope sc(s, MOE_STAGE_DISPATCH);
+      if ((e = launch_dispatch(topk_idx, T, E, k, d, s)) != cudaSuccess)
+        return cuda_fail(e, "dispatch");
+      if ((e = launch_gather_fp8(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), ue,
+                                 xq, xs, s)) != cudaSuccess)
+        return cuda_fail(e, "gather_fp8");
+      if ((e = cudaMemsetAsync(out32, 0, static_cast<size_t>(T) * H * 4, s)) != cudaSuccess)
+        return cuda_fail(e, "memset");
+    }
+    GroupedGemmFp8Args g{};
+    g.offsets = d.offsets;
+    g.tile_pref = d.tile_pref;
+    g.E = E;
+    g.I = I;
+    g.H = H;
+    g.k = k;
+    g.n_rows = static_cast<int>(n);
+    g.err = d.err;
+    g.ue8m0 = ue;
+    g.hq = hq;
+    g.hs = hs;
+    g.out32 = out32;
+    g.sorted_f = d.sorted_f;
+    g.topk_w = topk_w;
+    const long mtiles_max = n / kBM + E;
+    {
+      StageScope sc(s, MOE_STAGE_GEMM1);
+      g.tm_a = &tm_x;
+      g.tm_b = &tm_wgu;
+      g.K = H;
+      g.a_scale = xs;
+      g.w_scale = scale_gate_up;
+      g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
+      if ((e = launch_gemm1_fp8(g, s)) != cudaSuccess) return cuda_fail(e, "gemm1_fp8");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM2);
+      g.tm_a = &tm_h;
+      g.tm_b = &tm_wd;
+      g.K = I;
+      g.a_scale = hs;
+      g.w_scale = scale_down;
+      g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / 256)));
+      if ((e = launch_gemm2_fp8(g, s)) != cudaSuccess) return cuda_fail(e, "gemm2_fp8");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_FINISH);
+      if ((e = launch_to_bf16(out32, out, static_cast<long>(T) * H, s)) != cudaSuccess)
+        return cuda_fail(e, "to_bf16");
     }
     return MOE_OK;
   }

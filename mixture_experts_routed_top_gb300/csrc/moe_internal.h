@@ -105,6 +105,27 @@ cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 
 cudaError_t launch_gemm1_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+
+// FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
+struct GroupedGemmFp8Args {
+  const CUtensorMap* tm_a;   // e4m3 activations [n_rows, K], box 128 x 128 B
+  const CUtensorMap* tm_b;   // e4m3 weights [E * Nw, K], box 128 x 128 B
+  const int* offsets;
+  const int* tile_pref;
+  int E, K, I, H, k, n_rows;
+  int* err;
+  const void* a_scale;       // [K/128, n_rows]
+  const void* w_scale;       // [E, Nw/128, K/128]
+  bool ue8m0;
+  void* hq;                  // gate/up output codes [n_rows, I]
+  void* hs;                  // gate/up output scales [I/128, n_rows]
+  float* out32;              // down output accumulator [T, H]
+  const int* sorted_f;
+  const float* topk_w;
+  int num_sms;
+};
+cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
+cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 
 }  // namespace moe

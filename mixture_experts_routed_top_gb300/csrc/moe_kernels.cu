@@ -251,7 +251,9 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // Gather + dynamic 1x128 activation quantisation: one warp per row, each
-// lane owns 4 consecutive elements of every 128-wide block.
+// lane owns 4 consecutive elements of every 128-wide block.  Codes go to
+// xq[r, :], scales to xs[b, r] (K-block major, so that the GEMM epilogue's
+// per-row scale reads are coalesced).
 __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint2* __restrict__ hidden, int H,
                                                          int k, const int* __restrict__ sorted_f,
                                                          const int* __restrict__ nvalid, int rows,
@@ -277,9 +279,9 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint2* __restrict
     const uint32_t lo = e4m3x2(x0 * inv, x1 * inv);
     const uint32_t hi = e4m3x2(x2 * inv, x3 * inv);
     dst[b * 32 + lane] = lo | (hi << 16);
-    if (lane == 0) {
-      if (ue8m0) static_cast<uint8_t*>(xs)[r * nb + b] = static_cast<uint8_t>(stored);
-      else static_cast<uint32_t*>(xs)[r * nb + b] = stored;
+    if (lane == 0) {  // scales are K-block major: xs[b][r]
+      if (ue8m0) static_cast<uint8_t*>(xs)[static_cast<long>(b) * rows + r] = static_cast<uint8_t>(stored);
+      else static_cast<uint32_t*>(xs)[static_cast<long>(b) * rows + r] = stored;
     }
   }
 }
