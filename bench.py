@@ -219,12 +219,14 @@ class OracleSample:
     tokens of the workload, with only the experts those tokens select copied
     to the host (at most max_experts of them)."""
 
-    def __init__(self, w, n, max_experts=32):
+    def __init__(self, w, n, max_experts=None):
         import numpy as np
         import torch
         import oracle as O
         self.O, self.w = O, w
         s = w["shape"]
+        if max_experts is None:   # about 8 GB of host copies at float32
+            max_experts = max(8, int(8e9 // (3 * s.H * s.I * 4)))
         logits = w["logits"].float().cpu().numpy()
         idx_all, _ = O.route(logits, s.k)
         toks, ex = [], set()
@@ -287,6 +289,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.lib(build_if_missing=True)
+    moe.set_swap_rows({"auto": -1, "rows": 0, "swap": 1 << 20}[args.bf16_gemm])
     w = build_workload(args.workload, dev)
     s = w["shape"]
     W = weights_of(w)
@@ -419,6 +422,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("flushed before every timed step (512 MB write)" if flush else
                           f"inputs larger than L2 ({working_set / 1e9:.2f} GB touched per step)"),
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
+                   "bf16_gemm": args.bf16_gemm,
                    "workspace_bytes": ws_bytes},
         "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
         "weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
@@ -441,6 +445,8 @@ def main():
     ap.add_argument("--workload", default="qwen-prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-gemm", default="auto", choices=["auto", "rows", "swap"],
+                    help="orientation of the bf16 grouped GEMMs (library default: auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

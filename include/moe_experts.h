@@ -170,6 +170,20 @@ void moe_set_decode_rows(int rows);
 int moe_get_decode_rows(void);
 
 /*
+ * moe_set_swap_rows - choose the orientation of the bf16 grouped GEMMs.
+ * With T*k <= rows_per_expert * E (few routed rows per expert) the expert's
+ * weight rows are the MMA's M side and its tokens the N side (tokens padded
+ * to 16, "swap AB"); otherwise 128 token rows are the M side.  After a call
+ * with rows_per_expert >= 0 the rule applies to both GEMMs (0: token rows
+ * always).  The default (rows_per_expert < 0) applies it with 128 rows per
+ * expert to the gate/up GEMM and uses swap AB for the down GEMM at every
+ * size, the fastest combination measured on the benchmark workloads.
+ * Process-wide setting; moe_get_swap_rows returns the threshold in use.
+ */
+void moe_set_swap_rows(int rows_per_expert);
+int moe_get_swap_rows(void);
+
+/*
  * Stage timing: between moe_profile_begin() and moe_profile_end() every
  * launch of moe_experts_forward records a CUDA event pair on its stream
  * around each stage.  moe_profile_end() synchronises those events and writes

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
     "experts_forward", "quantize_fp8_blocks", "workspace_status", "set_decode_rows",
-    "get_decode_rows", "profile_begin", "profile_end", "selftest_wait_timeout", "launch_count",
+    "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "selftest_wait_timeout", "launch_count",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0",
 ]
@@ -54,6 +54,8 @@ _SIGS = {
     "moe_workspace_status": ([_P, _P], _I),
     "moe_set_decode_rows": ([_I], None),
     "moe_get_decode_rows": ([], _I),
+    "moe_set_swap_rows": ([_I], None),
+    "moe_get_swap_rows": ([], _I),
     "moe_profile_begin": ([], _I),
     "moe_profile_end": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
     "moe_selftest_wait_timeout": ([_P, _SZ, _I, _P], _I),
@@ -243,6 +245,16 @@ def set_decode_rows(rows: int):
 
 def get_decode_rows() -> int:
     return int(lib().moe_get_decode_rows())
+
+
+def set_swap_rows(rows_per_expert: int):
+    """Mean rows per expert at or below which the bf16 GEMMs use the swap-AB
+    orientation (< 0: default, 0: never)."""
+    lib().moe_set_swap_rows(int(rows_per_expert))
+
+
+def get_swap_rows() -> int:
+    return int(lib().moe_get_swap_rows())
 
 
 def profile_begin():

@@ -1,4 +1,6 @@
-// Grouped tensor-core GEMMs of the routed experts forward on sm_103a.
+// Grouped tensor-core GEMMs (bf16), token-row orientation, for experts with
+// many routed rows (prefill).  The swap-AB kernel in gemm_grouped.cu covers
+// experts with few rows.
 //
 // Rows of the activation matrix are expert-contiguous (the dispatch step);
 // expert e owns rows [offsets[e], offsets[e+1]).  The work is cut into tiles
@@ -80,7 +82,7 @@ __device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* 
 
 template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a,
+    grouped_gemm_rows_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, const GemmDev p) {
   using L = Layout<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int EPI, int BN>
 cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   using L = Layout<BN>;
-  auto kern = grouped_gemm_bf16_kernel<EPI, BN>;
+  auto kern = grouped_gemm_rows_kernel<EPI, BN>;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -334,11 +336,13 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_gemm1_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+// tm_a: activations (box 128 rows), tm_b: weights (box 128 rows),
+// tile_pref: prefix of ceil(M_e / 128).
+cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_impl<EPI_SWIGLU, 256>(a, s);
 }
 
-cudaError_t launch_gemm2_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.H % 256 == 0) return launch_impl<EPI_COMBINE, 256>(a, s);
   return launch_impl<EPI_COMBINE, 128>(a, s);
 }

@@ -60,6 +60,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int g_decode_rows = -1;  // < 0: default
+int g_swap_rows = -1;    // < 0: default
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -71,7 +72,7 @@ struct WsLayout {
 WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
   WsLayout L{};
   const long n = T * k;
-  const long nchunks = n ? (n + kDispatchChunk - 1) / kDispatchChunk : 0;
+  const long nchunks = n ? (n + dispatch_chunk(n) - 1) / dispatch_chunk(n) : 0;
   size_t off = sizeof(WsHeader);
   auto take = [&](size_t bytes) {
     size_t at = align_up(off, 1024);
@@ -98,7 +99,7 @@ WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
 
 size_t dispatch_ws_bytes(long T, long E, long k) {
   const long n = T * k;
-  const long nchunks = n ? (n + kDispatchChunk - 1) / kDispatchChunk : 0;
+  const long nchunks = n ? (n + dispatch_chunk(n) - 1) / dispatch_chunk(n) : 0;
   size_t off = align_up(sizeof(WsHeader), 1024);
   off = align_up(off + (E + 1) * 4, 1024);  // tile prefix
   off = align_up(off + (E + 1) * 4, 1024);  // touched list
@@ -121,15 +122,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major [outer, inner] matrix, box = 128 rows x 128 bytes, 128-byte
-// swizzle, out-of-range rows read as zero.
+// 2-D row-major [outer, inner] matrix, box = box_rows rows x 128 bytes,
+// 128-byte swizzle, out-of-range rows read as zero.
 moe_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
-                    uint64_t inner, uint64_t outer) {
+                    uint64_t inner, uint64_t outer, uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * esize};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 128};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -200,6 +201,9 @@ void moe_set_decode_rows(int rows) {
   g_decode_rows = rows < 0 ? -1 : (rows > kDecodeRowsMax ? kDecodeRowsMax : rows);
 }
 int moe_get_decode_rows(void) { return g_decode_rows < 0 ? kDecodeRowsDefault : g_decode_rows; }
+
+void moe_set_swap_rows(int rows_per_expert) { g_swap_rows = rows_per_expert < 0 ? -1 : rows_per_expert; }
+int moe_get_swap_rows(void) { return g_swap_rows < 0 ? kSwapRowsDefault : g_swap_rows; }
 
 moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                      void* stream) {
@@ -381,8 +385,9 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
       return st;
     {
       StageScope sc(s, MOE_STAGE_DISPATCH);
-      if ((e = launch_dispatch(topk_idx, T, E, k, d, s)) != cudaSuccess)
-        return cuda_fail(e, "dispatch");
+      e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
+                                 : launch_dispatch(topk_idx, T, E, k, d, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dispatch");
       if ((e = launch_gather_fp8(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), ue,
                                  xq, xs, s)) != cudaSuccess)
         return cuda_fail(e, "gather_fp8");
@@ -433,20 +438,33 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     return MOE_OK;
   }
 
+  // Orientation of each grouped GEMM.  Gate/up: weight rows as the MMA's M
+  // side (swap-AB) when experts get few rows, token rows as M otherwise.
+  // Down: swap-AB (measured faster at every size) unless a threshold was set
+  // explicitly, which then applies to both (0: token rows always).
+  const int swap_rows = moe_get_swap_rows();
+  const bool swap1 = n <= static_cast<long>(swap_rows) * E;
+  const bool swap2 = g_swap_rows >= 0 ? swap1 : true;
   CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
   moe_status st;
-  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n)) != MOE_OK) return st;
+  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, swap1 ? 64 : 128)) !=
+      MOE_OK)
+    return st;
   if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
                      static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
     return st;
-  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n)) != MOE_OK) return st;
+  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, swap2 ? 64 : 128)) !=
+      MOE_OK)
+    return st;
   if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
                      static_cast<uint64_t>(E) * H)) != MOE_OK)
     return st;
 
   {
     StageScope sc(s, MOE_STAGE_DISPATCH);
-    if ((e = launch_dispatch(topk_idx, T, E, k, d, s)) != cudaSuccess) return cuda_fail(e, "dispatch");
+    e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
+                               : launch_dispatch(topk_idx, T, E, k, d, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dispatch");
     if ((e = launch_gather_bf16(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), xa,
                                 s)) != cudaSuccess)
       return cuda_fail(e, "gather");
@@ -469,20 +487,22 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
   const long mtiles_max = n / kBM + E;
   {
     StageScope sc(s, MOE_STAGE_GEMM1);
-    g.tm_a = &tm_x;
-    g.tm_b = &tm_wgu;
+    g.tm_a = swap1 ? &tm_wgu : &tm_x;
+    g.tm_b = swap1 ? &tm_x : &tm_wgu;
     g.K = H;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
-    if ((e = launch_gemm1_bf16(g, s)) != cudaSuccess) return cuda_fail(e, "gemm1");
+    e = swap1 ? launch_gemm1_bf16_swap(g, s) : launch_gemm1_bf16_rows(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm1");
   }
   {
     StageScope sc(s, MOE_STAGE_GEMM2);
-    g.tm_a = &tm_h;
-    g.tm_b = &tm_wd;
+    g.tm_a = swap2 ? &tm_wd : &tm_h;
+    g.tm_b = swap2 ? &tm_h : &tm_wd;
     g.K = I;
-    const int bn = (H % 256 == 0) ? 256 : 128;
-    g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / bn)));
-    if ((e = launch_gemm2_bf16(g, s)) != cudaSuccess) return cuda_fail(e, "gemm2");
+    const int nf = (H % 256 == 0) ? 256 : 128;
+    g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / nf)));
+    e = swap2 ? launch_gemm2_bf16_swap(g, s) : launch_gemm2_bf16_rows(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm2");
   }
   {
     StageScope sc(s, MOE_STAGE_FINISH);

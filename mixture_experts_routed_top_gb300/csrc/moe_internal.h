@@ -21,8 +21,14 @@ enum : int {
 
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
-constexpr int kDispatchChunk = 2048;   // routing entries per histogram/permute block
-constexpr int kBM = 128;               // token rows per grouped-GEMM tile
+// Routing entries per histogram/placement block: at least 256, and at most
+// 128 blocks whatever T*k is (the scan walks the blocks serially).
+inline long dispatch_chunk(long n) {
+  const long c = (n + 127) / 128;
+  return c <= 256 ? 256 : (c + 255) / 256 * 256;
+}
+constexpr int kSmallDispatchMax = 2048;  // T*k at or below: one-CTA dispatch
+constexpr int kBM = 128;               // max token rows per grouped-GEMM tile
 
 // Device-side error word block at the head of every workspace.
 struct WsHeader {
@@ -65,10 +71,15 @@ cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, 
                                    uint8_t* q, void* scale, cudaStream_t s);
 cudaError_t launch_selftest_wait(int* err, int limit_us, cudaStream_t s);
 
-// Grouped tensor-core GEMMs.
+// Grouped tensor-core GEMMs (bf16).  Two orientations: token rows as the
+// MMA's M side (gemm_rows.cu: tm_a = activations, tm_b = weights, both
+// 128-row boxes) for experts with many rows, and weight rows as M
+// (gemm_swap.cu: tm_a = weights with 128-row boxes, tm_b = activations with
+// 64-row boxes) for experts with few rows.  Both use tile_pref = prefix of
+// ceil(M_e / 128).
 struct GroupedGemmArgs {
-  const CUtensorMap* tm_a;   // activations [rows, K], box 128 rows
-  const CUtensorMap* tm_b;   // weights [E * Nw, K], box 128 rows
+  const CUtensorMap* tm_a;
+  const CUtensorMap* tm_b;
   const int* offsets;        // [E+1]
   const int* tile_pref;      // [E+1]
   int E, K, I, H, k;
@@ -81,6 +92,33 @@ struct GroupedGemmArgs {
   const float* topk_w;
   int num_sms;
 };
+cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm1_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
+
+// FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
+struct GroupedGemmFp8Args {
+  const CUtensorMap* tm_a;   // e4m3 activations [n_rows, K], box 128 x 128 B
+  const CUtensorMap* tm_b;   // e4m3 weights [E * Nw, K], box 128 x 128 B
+  const int* offsets;
+  const int* tile_pref;
+  int E, K, I, H, k, n_rows;
+  int* err;
+  const void* a_scale;       // [K/128, n_rows]
+  const void* w_scale;       // [E, Nw/128, K/128]
+  bool ue8m0;
+  void* hq;                  // gate/up output codes [n_rows, I]
+  void* hs;                  // gate/up output scales [I/128, n_rows]
+  float* out32;              // down output accumulator [T, H]
+  const int* sorted_f;
+  const float* topk_w;
+  int num_sms;
+};
+cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
+cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
+
 // Small-token decode path.
 struct DecodeArgs {
   const void* hidden;        // bf16 [T, H]
@@ -103,29 +141,5 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
-
-cudaError_t launch_gemm1_bf16(const GroupedGemmArgs& a, cudaStream_t s);
-
-// FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
-struct GroupedGemmFp8Args {
-  const CUtensorMap* tm_a;   // e4m3 activations [n_rows, K], box 128 x 128 B
-  const CUtensorMap* tm_b;   // e4m3 weights [E * Nw, K], box 128 x 128 B
-  const int* offsets;
-  const int* tile_pref;
-  int E, K, I, H, k, n_rows;
-  int* err;
-  const void* a_scale;       // [K/128, n_rows]
-  const void* w_scale;       // [E, Nw/128, K/128]
-  bool ue8m0;
-  void* hq;                  // gate/up output codes [n_rows, I]
-  void* hs;                  // gate/up output scales [I/128, n_rows]
-  float* out32;              // down output accumulator [T, H]
-  const int* sorted_f;
-  const float* topk_w;
-  int num_sms;
-};
-cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
-cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
-cudaError_t launch_gemm2_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 
 }  // namespace moe

@@ -96,13 +96,13 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
 // word, so no later kernel ever indexes with them.
 
 __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ idx,
-                                                             long n, int E, int* blk_counts,
-                                                             int* err) {
+                                                             long n, long chunk, int E,
+                                                             int* blk_counts, int* err) {
   __shared__ int hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const long base = static_cast<long>(blockIdx.x) * kDispatchChunk;
-  const long end = min(base + kDispatchChunk, n);
+  const long base = static_cast<long>(blockIdx.x) * chunk;
+  const long end = min(base + chunk, n);
   bool bad = false;
   for (long f = base + threadIdx.x; f < end; f += blockDim.x) {
     const int e = __ldg(idx + f);
@@ -115,20 +115,37 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
     blk_counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
 }
 
+// Per-chunk counts -> per-chunk write bases.  Warp w handles experts w,
+// w+32, ...: its lanes read that expert's chunk counts 32 chunks at a time
+// (independent loads in flight) and a warp scan carries the running base.
+// Then one block-wide scan over experts gives counts, offsets, the m-tile
+// prefix and the touched list, and the bases are shifted by the offsets.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks, int* blk_counts,
                                                              int* counts, int* offsets,
                                                              int* tile_pref, int* touched) {
   __shared__ int s_warp[33];
-  const int e = threadIdx.x;
-  int c = 0;
-  if (e < E) {
-    for (int b = 0; b < nchunks; ++b) {
+  __shared__ int s_tot[kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += 32) {
+    int carry = 0;
+    for (int b0 = 0; b0 < nchunks; b0 += 32) {
+      const int b = b0 + lane;
       const long i = static_cast<long>(b) * E + e;
-      const int v = blk_counts[i];
-      blk_counts[i] = c;
-      c += v;
+      const int v = b < nchunks ? blk_counts[i] : 0;
+      int x = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (b < nchunks) blk_counts[i] = carry + x - v;   // exclusive within the expert
+      carry += __shfl_sync(0xffffffffu, x, 31);
     }
+    if (lane == 0) s_tot[e] = carry;
   }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = e < E ? s_tot[e] : 0;
   const int tiles = (c + kBM - 1) / kBM;
   const int tch = c > 0 ? 1 : 0;
   int tot_c, tot_t, tot_h;
@@ -140,24 +157,28 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks,
     offsets[e] = ex_c;
     tile_pref[e] = ex_t;
     if (tch) touched[1 + ex_h] = e;
-    for (int b = 0; b < nchunks; ++b) blk_counts[static_cast<long>(b) * E + e] += ex_c;
+    s_tot[e] = ex_c;
   }
   if (e == 0) {
     offsets[E] = tot_c;
     tile_pref[E] = tot_t;
     touched[0] = tot_h;
   }
+  __syncthreads();
+  // shift the per-chunk bases by the expert offsets (coalesced over experts)
+  const long total = static_cast<long>(nchunks) * E;
+  for (long i = threadIdx.x; i < total; i += 1024) blk_counts[i] += s_tot[i % E];
 }
 
 __global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __restrict__ idx, long n,
-                                                            int E, const int* blk_base,
+                                                            long chunk, int E, const int* blk_base,
                                                             int* sorted_f, int* row_of) {
   __shared__ int cursor[kMaxE];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) cursor[e] = blk_base[static_cast<long>(blockIdx.x) * E + e];
   __syncwarp();
-  const long base = static_cast<long>(blockIdx.x) * kDispatchChunk;
-  const long end = min(base + kDispatchChunk, n);
+  const long base = static_cast<long>(blockIdx.x) * chunk;
+  const long end = min(base + chunk, n);
   const uint32_t lt = (1u << lane) - 1u;
   for (long f0 = base; f0 < end; f0 += 32) {
     const long f = f0 + lane;
@@ -179,15 +200,16 @@ __global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __res
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const DispatchBufs& d,
                             cudaStream_t s) {
   const long n = static_cast<long>(T) * k;
-  const int nchunks = n ? ceil_div(n, kDispatchChunk) : 0;
+  const long chunk = dispatch_chunk(n);
+  const int nchunks = n ? ceil_div(n, chunk) : 0;
   if (nchunks) {
-    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, n, E, d.blk_counts, d.err);
+    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, n, chunk, E, d.blk_counts, d.err);
   }
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(E, nchunks, d.blk_counts, d.counts, d.offsets,
                                           d.tile_pref, d.touched);
   if (nchunks) {
-    dispatch_place_kernel<<<nchunks, 32, 0, s>>>(topk_idx, n, E, d.blk_counts, d.sorted_f,
-                                                 d.row_of);
+    dispatch_place_kernel<<<nchunks, 32, 0, s>>>(topk_idx, n, chunk, E, d.blk_counts,
+                                                 d.sorted_f, d.row_of);
   }
   count_launches(nchunks ? 3 : 1);
   return cudaGetLastError();

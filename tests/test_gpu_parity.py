@@ -92,15 +92,21 @@ def test_dispatch_out_of_range_index_is_reported(moe):
 
 
 # ----------------------------------------------------------------- forward
-PATHS = {"prefill": 0, "decode": 2048}
+# (decode-path row threshold, swap-AB rows-per-expert threshold)
+PATHS = {"rows": (0, 0), "swap": (0, 1 << 20), "decode": (2048, -1)}
 
 
 @pytest.fixture
 def path(moe, request):
-    """Force the grouped tensor-core path or the decode path."""
-    moe.set_decode_rows(PATHS[request.param])
+    """Force one of the three bf16 paths: grouped GEMMs with token rows as
+    the MMA's M side, grouped GEMMs with weight rows as M (swap-AB), or the
+    decode GEMVs."""
+    dec, swap = PATHS[request.param]
+    moe.set_decode_rows(dec)
+    moe.set_swap_rows(swap)
     yield request.param
     moe.set_decode_rows(-1)
+    moe.set_swap_rows(-1)
 
 
 def _forward_case(moe, shape, seed=0, logit_bias=None, device_inputs=None):
@@ -129,7 +135,7 @@ SMALL_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap", "decode"], indirect=True)
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 def test_forward_bf16_parity(moe, shape, path):
     out, ref = _forward_case(moe, shape)
@@ -138,34 +144,37 @@ def test_forward_bf16_parity(moe, shape, path):
     assert np.all(np.isfinite(out))
 
 
-@pytest.mark.parametrize("path", ["prefill"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap"], indirect=True)
 def test_forward_bf16_parity_qwen_shape_520_tokens(moe, path):
     out, ref = _forward_case(moe, MoEShape(T=520, H=2048, I=1408, E=60, k=4))
     assert O.rel_max_err(out, ref) <= BF16_TOL
 
 
-@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap", "decode"], indirect=True)
 def test_forward_bf16_one_expert_takes_all(moe, path):
-    shape = MoEShape(T=700 if path == "prefill" else 90, H=256, I=256, E=8, k=2)
+    shape = MoEShape(T=700 if path != "decode" else 90, H=256, I=256, E=8, k=2)
     bias = torch.zeros(8)
     bias[5] = 30.0                                  # every token routes to expert 5
     out, ref = _forward_case(moe, shape, logit_bias=bias)
     assert O.rel_max_err(out, ref) <= BF16_TOL
 
 
-def test_decode_and_prefill_paths_agree(moe):
+def test_all_paths_agree(moe):
     shape = MoEShape(T=96, H=512, I=384, E=16, k=4)
     d = make_inputs(shape, seed=5, device="cuda")
     idx, w = moe.route(d["logits"], shape.k)
     outs = []
-    for rows in (0, 2048):
-        moe.set_decode_rows(rows)
+    for dec, swap in PATHS.values():
+        moe.set_decode_rows(dec)
+        moe.set_swap_rows(swap)
         outs.append(moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"]).float())
     moe.set_decode_rows(-1)
+    moe.set_swap_rows(-1)
     # different accumulation orders: a one-ulp bf16 flip at the largest
     # outputs is ~1.7 % of rms, so the bound is the parity tolerance
     ref = outs[0].pow(2).mean().sqrt().item()
-    assert (outs[0] - outs[1]).abs().max().item() <= BF16_TOL * ref
+    for o in outs[1:]:
+        assert (outs[0] - o).abs().max().item() <= BF16_TOL * ref
 
 
 @pytest.mark.parametrize("T", [1, 8, 32, 128])
@@ -252,7 +261,7 @@ def test_forward_rejects_unsupported(moe):
     assert ei.value.status == 2
 
 
-@pytest.mark.parametrize("path", ["prefill", "decode"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap", "decode"], indirect=True)
 def test_forward_bad_expert_index_reported(moe, path):
     shape = MoEShape(T=16, H=128, I=128, E=4, k=2)
     d = make_inputs(shape, seed=1, device="cuda")

@@ -51,7 +51,8 @@ def test_dispatch_noalloc_rejects_sizes_beyond_its_scratch():
     fn = _entry(L)
     nul = ctypes.c_void_p(0)
     n0 = moe.launch_count()
-    st = fn(nul, 10_000_000, 256, 8, nul, nul, nul, nul, nul)
+    # 128 histogram blocks x 4096 experts x 4 B = 2 MiB of scratch > 1 MiB
+    st = fn(nul, 10_000_000, 4096, 8, nul, nul, nul, nul, nul)
     assert st == 2
     assert b"scratch" in L.moe_last_error()
     assert moe.launch_count() == n0
