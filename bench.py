@@ -319,28 +319,45 @@ def run_ours(args, rank, world, local_rank):
         step(w["logits"], w["hidden"])
     torch.cuda.synchronize()
 
+    graph = None
+    if args.graph:
+        # One step captured as a CUDA graph (router + forward, all kernels of
+        # the library); the per-stage CUDA events are captured with it.
+        moe.profile_begin()
+        n_cap = moe.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(w["logits"], w["hidden"])
+        per_step_launches = moe.launch_count() - n_cap
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     n0 = moe.launch_count()
-    moe.profile_begin()
+    if graph is None:
+        moe.profile_begin()
     with ClockSampler(dev.index) as clk:
-        t_wall0 = time.perf_counter()
         for i in range(args.steps):
             if flush:
                 flush_buf.zero_()
             starts[i].record(stream)
-            step(w["logits"], w["hidden"])
+            if graph is not None:
+                graph.replay()
+            else:
+                step(w["logits"], w["hidden"])
             ends[i].record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # with a graph the captured stage events hold the last replay's times
     stages = moe.profile_end()
-    launches = moe.launch_count() - n0
+    launches = (per_step_launches * args.steps) if graph is not None else moe.launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(step_ms)
     if world > 1:
@@ -423,6 +440,8 @@ def run_ours(args, rank, world, local_rank):
                           f"inputs larger than L2 ({working_set / 1e9:.2f} GB touched per step)"),
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
                    "bf16_gemm": args.bf16_gemm,
+                   "timed_steps": "CUDA graph replays of one captured step" if args.graph
+                                  else "steps launched from Python",
                    "workspace_bytes": ws_bytes},
         "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
         "weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
@@ -445,6 +464,8 @@ def main():
     ap.add_argument("--workload", default="qwen-prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every timed step from Python instead of replaying a CUDA graph")
     ap.add_argument("--bf16-gemm", default="auto", choices=["auto", "rows", "swap"],
                     help="orientation of the bf16 grouped GEMMs (library default: auto)")
     args = ap.parse_args()

@@ -2,6 +2,8 @@
 // stream over the touched experts' weights, so it runs on CUDA cores as
 // GEMVs that read every touched weight row exactly once (the page's
 // "Decode-stage switching" idea: a separate strategy for low token counts).
+// Up to kFusedDecodeRows routed rows the path is two kernels (fused at the
+// end of this file); above that it is the four below.
 //
 //   dispatch_small   one CTA: counts, scan, touched list, stable placement
 //   decode_gate_up   item = (touched expert, 4 features); warp = feature f:
@@ -77,14 +79,9 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
 }
 
 // ------------------------------------------------------------ helpers
-// Weights are read once: bypass L1.
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+// Weights are read once: cache-streaming loads, which the compiler can
+// batch ahead of the arithmetic that consumes them.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -99,6 +96,86 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8], 
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
   return acc;
+}
+
+constexpr int kStreamBatch = 8;  // 16-byte weight vectors per lane loaded before any math
+
+// ag[t] += w_gate . x_t and au[t] += w_up . x_t over 16-byte vectors
+// lane, lane+32, ... < n8 of two weight rows; each lane first issues
+// kStreamBatch loads per row, then does the arithmetic.
+template <int MT>
+__device__ __forceinline__ void stream_dot2(const uint4* __restrict__ wg,
+                                            const uint4* __restrict__ wu,
+                                            const uint4* const (&xr)[MT], int n8, int lane,
+                                            float (&ag)[MT], float (&au)[MT]) {
+  int c0 = lane;
+  for (; c0 + 32 * (kStreamBatch - 1) < n8; c0 += 32 * kStreamBatch) {
+    uint4 g[kStreamBatch], u[kStreamBatch];
+#pragma unroll
+    for (int i = 0; i < kStreamBatch; ++i) {
+      g[i] = ld_stream(wg + c0 + 32 * i);
+      u[i] = ld_stream(wu + c0 + 32 * i);
+    }
+#pragma unroll
+    for (int i = 0; i < kStreamBatch; ++i) {
+      float gf[8], uf[8];
+      bf16x8_to_f32(g[i], gf);
+      bf16x8_to_f32(u[i], uf);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        float xf[8];
+        bf16x8_to_f32(__ldg(xr[t] + c0 + 32 * i), xf);
+        ag[t] = dot8(gf, xf, ag[t]);
+        au[t] = dot8(uf, xf, au[t]);
+      }
+    }
+  }
+  for (; c0 < n8; c0 += 32) {
+    float gf[8], uf[8];
+    bf16x8_to_f32(ld_stream(wg + c0), gf);
+    bf16x8_to_f32(ld_stream(wu + c0), uf);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float xf[8];
+      bf16x8_to_f32(__ldg(xr[t] + c0), xf);
+      ag[t] = dot8(gf, xf, ag[t]);
+      au[t] = dot8(uf, xf, au[t]);
+    }
+  }
+}
+
+// acc[t] += w . x_t over one weight row, batched the same way.
+template <int MT>
+__device__ __forceinline__ void stream_dot1(const uint4* __restrict__ w,
+                                            const uint4* const (&xr)[MT], int n8, int lane,
+                                            float (&acc)[MT]) {
+  int c0 = lane;
+  for (; c0 + 32 * (kStreamBatch - 1) < n8; c0 += 32 * kStreamBatch) {
+    uint4 v[kStreamBatch];
+#pragma unroll
+    for (int i = 0; i < kStreamBatch; ++i) v[i] = ld_stream(w + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < kStreamBatch; ++i) {
+      float wf[8];
+      bf16x8_to_f32(v[i], wf);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        float xf[8];
+        bf16x8_to_f32(__ldg(xr[t] + c0 + 32 * i), xf);
+        acc[t] = dot8(wf, xf, acc[t]);
+      }
+    }
+  }
+  for (; c0 < n8; c0 += 32) {
+    float wf[8];
+    bf16x8_to_f32(ld_stream(w + c0), wf);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float xf[8];
+      bf16x8_to_f32(__ldg(xr[t] + c0), xf);
+      acc[t] = dot8(wf, xf, acc[t]);
+    }
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -136,19 +213,7 @@ __global__ void __launch_bounds__(128) decode_gate_up_kernel(
       float ag[MT], au[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) ag[t] = au[t] = 0.f;
-#pragma unroll 4
-      for (int c = lane; c < H8; c += 32) {
-        float gf[8], uf[8];
-        bf16x8_to_f32(ld_stream(wg + c), gf);
-        bf16x8_to_f32(ld_stream(wu + c), uf);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          float xf[8];
-          bf16x8_to_f32(__ldg(xr[t] + c), xf);
-          ag[t] = dot8(gf, xf, ag[t]);
-          au[t] = dot8(uf, xf, au[t]);
-        }
-      }
+      stream_dot2<MT>(wg, wu, xr, H8, lane, ag, au);
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const float g = warp_sum(ag[t]);
@@ -184,17 +249,7 @@ __global__ void __launch_bounds__(128) decode_down_kernel(
       float acc[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) acc[t] = 0.f;
-#pragma unroll 4
-      for (int v = lane; v < I8; v += 32) {
-        float wf[8];
-        bf16x8_to_f32(ld_stream(wr + v), wf);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          float xf[8];
-          bf16x8_to_f32(__ldg(hr[t] + v), xf);
-          acc[t] = dot8(wf, xf, acc[t]);
-        }
-      }
+      stream_dot1<MT>(wr, hr, I8, lane, acc);
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const float y = warp_sum(acc[t]);
@@ -229,6 +284,147 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __res
       s.w += y.w;
     }
     out[i] = make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+  }
+}
+
+// ------------------------------------------------------------ fused (tiny T*k)
+// For T*k <= kFusedDecodeRows every CTA rebuilds the routing table itself in
+// shared memory (stable order by expert, touched list), so no dispatch
+// kernel runs; the down GEMV also sums the k contributions of each token in
+// place, so no combine kernel runs either.
+struct SmallTable {
+  int sf[kFusedDecodeRows];       // row r -> flat entry f (stable, by expert)
+  int te[kFusedDecodeRows];       // touched experts, ascending
+  int tb[kFusedDecodeRows + 1];   // first row of each touched expert (+ end)
+  int nt;                         // number of touched experts
+  int idx[kFusedDecodeRows];
+};
+
+// All threads of the block call this; blockDim.x >= n.
+__device__ void build_small_table(const int32_t* __restrict__ topk_idx, int n, int E,
+                                  SmallTable& t, int* err) {
+  const int tid = threadIdx.x;
+  if (tid < n) t.idx[tid] = __ldg(topk_idx + tid);
+  __syncthreads();
+  if (tid < n) {
+    const int e = t.idx[tid];
+    if (e >= 0 && e < E) {
+      int rank = 0;
+      for (int f2 = 0; f2 < n; ++f2) {
+        const int e2 = t.idx[f2];
+        rank += (e2 >= 0 && e2 < E) && (e2 < e || (e2 == e && f2 < tid));
+      }
+      t.sf[rank] = tid;
+    } else if (blockIdx.x == 0) {
+      atomicOr(err, ERR_BAD_INDEX);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int nv = 0;
+    for (int f = 0; f < n; ++f) nv += t.idx[f] >= 0 && t.idx[f] < E;
+    int nt = 0, prev = -1;
+    for (int r = 0; r < nv; ++r) {
+      const int e = t.idx[t.sf[r]];
+      if (e != prev) {
+        t.te[nt] = e;
+        t.tb[nt] = r;
+        ++nt;
+        prev = e;
+      }
+    }
+    t.tb[nt] = nv;
+    t.nt = nt;
+  }
+  __syncthreads();
+}
+
+template <int MT>
+__global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
+    const __nv_bfloat16* __restrict__ hidden, int H, int I, int k, int E, int n,
+    const __nv_bfloat16* __restrict__ wgu, const int32_t* __restrict__ topk_idx,
+    __nv_bfloat16* __restrict__ h_out, int* err) {
+  __shared__ SmallTable tab;
+  build_small_table(topk_idx, n, E, tab, err);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_e = I / 4;
+  const int n_items = tab.nt * per_e;
+  const int H8 = H / 8;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int j = item / per_e;
+    const int e = tab.te[j];
+    const int f = (item - j * per_e) * 4 + warp;
+    const int r0 = tab.tb[j];
+    const int m = tab.tb[j + 1] - r0;
+    const uint4* wg = reinterpret_cast<const uint4*>(wgu + (static_cast<long>(e) * 2 * I + f) * H);
+    const uint4* wu = reinterpret_cast<const uint4*>(wgu + (static_cast<long>(e) * 2 * I + I + f) * H);
+    for (int t0 = 0; t0 < m; t0 += MT) {
+      const uint4* xr[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t)
+        xr[t] = reinterpret_cast<const uint4*>(hidden) +
+                static_cast<long>(tab.sf[r0 + min(t0 + t, m - 1)] / k) * H8;
+      float ag[MT], au[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) ag[t] = au[t] = 0.f;
+      stream_dot2<MT>(wg, wu, xr, H8, lane, ag, au);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const float gs = warp_sum(ag[t]);
+        const float us = warp_sum(au[t]);
+        if (lane == 0 && t0 + t < m)
+          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(silu_f(gs) * us);
+      }
+    }
+  }
+}
+
+// One output column per block: its four warps split the touched experts,
+// each streaming W_down[e, c, :] once and adding w * y per token into its
+// shared-memory row; the block then sums the four rows and writes the bf16
+// outputs of the column.
+template <int MT>
+__global__ void __launch_bounds__(128) decode_fused_down_kernel(
+    const __nv_bfloat16* __restrict__ h, int T, int H, int I, int k, int E, int n,
+    const __nv_bfloat16* __restrict__ wd, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, __nv_bfloat16* __restrict__ out, int* err) {
+  __shared__ SmallTable tab;
+  __shared__ float s_acc[4][kFusedDecodeRows];
+  build_small_table(topk_idx, n, E, tab, err);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int I8 = I / 8;
+  for (int c = blockIdx.x; c < H; c += gridDim.x) {
+    for (int t = lane; t < T; t += 32) s_acc[warp][t] = 0.f;
+    __syncwarp();
+    for (int j = warp; j < tab.nt; j += 4) {
+      const int e = tab.te[j];
+      const int r0 = tab.tb[j];
+      const int m = tab.tb[j + 1] - r0;
+      const uint4* wr = reinterpret_cast<const uint4*>(wd + (static_cast<long>(e) * H + c) * I);
+      for (int t0 = 0; t0 < m; t0 += MT) {
+        const uint4* hr[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+          hr[t] = reinterpret_cast<const uint4*>(h) + static_cast<long>(r0 + min(t0 + t, m - 1)) * I8;
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+        stream_dot1<MT>(wr, hr, I8, lane, acc);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const float y = warp_sum(acc[t]);
+          if (lane == 0 && t0 + t < m) {
+            const int f = tab.sf[r0 + t0 + t];
+            s_acc[warp][f / k] += y * __ldg(topk_w + f);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += 128)
+      out[static_cast<long>(t) * H + c] =
+          __float2bfloat16_rn(s_acc[0][t] + s_acc[1][t] + s_acc[2][t] + s_acc[3][t]);
+    __syncthreads();
   }
 }
 
@@ -275,6 +471,42 @@ cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s) {
     case 4: decode_down_kernel<4><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
     case 2: decode_down_kernel<2><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
     default: decode_down_kernel<1><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk_idx, int* err,
+                                       cudaStream_t s) {
+  const int n = a.T * a.k;
+  const int grid = decode_grid(a, a.I / 4);
+  auto* hb = static_cast<__nv_bfloat16*>(a.h);
+  auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
+  auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
+  switch (mt_for(a.T)) {
+    case 8: decode_fused_gate_up_kernel<8><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 4: decode_fused_gate_up_kernel<4><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 2: decode_fused_gate_up_kernel<2><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    default: decode_fused_gate_up_kernel<1><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_idx, int* err,
+                                     cudaStream_t s) {
+  const int n = a.T * a.k;
+  const long want = a.H;
+  const long slots = static_cast<long>(a.num_sms) * 16;
+  const int grid = static_cast<int>(want < slots ? want : slots);
+  auto* hb = static_cast<const __nv_bfloat16*>(a.h);
+  auto* w = static_cast<const __nv_bfloat16*>(a.w_down);
+  auto* o = static_cast<__nv_bfloat16*>(a.out);
+  switch (mt_for(a.T)) {
+    case 8: decode_fused_down_kernel<8><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    case 4: decode_fused_down_kernel<4><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    case 2: decode_fused_down_kernel<2><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    default: decode_fused_down_kernel<1><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
   }
   count_launches(1);
   return cudaGetLastError();

@@ -11,18 +11,19 @@
 // accumulators with the block's scale product.  Two 256-column TMEM buffers
 // let the MMA of K-block kb+1 run while K-block kb is being promoted.
 //
-// Roles (persistent, one CTA per SM, 320 threads):
-//   warp 0      TMA producer, 4-stage ring of A 128x128 B + B 256x128 B
-//   warp 1      TMEM allocator + MMA issuer
-//   warps 2-9   epilogue: warpgroup 0 = warps 2-5, warpgroup 1 = warps 6-9;
-//               thread = tile row (TMEM lane), warpgroup = half of the columns
-//     gate/up:  warpgroup g owns gate columns 64g..64g+63 and the matching up
-//               columns; at tile end h = silu(g)*u is re-quantised per row
-//               over the tile's 128 columns (one 1x128 block of I; the two
-//               warpgroups exchange their row maxima through shared memory)
-//     down:     warpgroup g owns output columns 128g..128g+127 (one weight
-//               block row); at tile end y * routing weight is added into the
-//               fp32 accumulator of the token (vector atomics)
+// Roles (persistent, one CTA per SM, 576 threads):
+//   warp 0       TMA producer, 4-stage ring of A 128x128 B + B 256x128 B
+//   warp 1       TMEM allocator + MMA issuer
+//   warps 2-17   epilogue, four warpgroups (warps 2-5, 6-9, 10-13, 14-17);
+//                thread = tile row (TMEM lane), warpgroup = a quarter of the
+//                columns, so the per-K-block promotion is spread over 16 warps
+//     gate/up:   warpgroup g owns gate columns 32g..32g+31 and the matching up
+//                columns; at tile end h = silu(g)*u is re-quantised per row
+//                over the tile's 128 columns (one 1x128 block of I; the four
+//                warpgroups exchange their row maxima through shared memory)
+//     down:      warpgroup g owns output columns 64g..64g+63 (inside weight
+//                block row g/2); at tile end y * routing weight is added into
+//                the fp32 accumulator of the token (vector atomics)
 // All waits are bounded as in the bf16 kernel.
 #include <cuda_fp8.h>
 
@@ -36,7 +37,9 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // e4m3 per 128-byte row = one scale block
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiGroups = kEpiWarps / 4;
+constexpr int kGroupCols = 256 / kEpiGroups;  // partial-sum columns per warpgroup
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kBufCols = 256;
@@ -52,8 +55,8 @@ struct L8 {
   static constexpr int OFF_BAR = OFF_B + kStages * B_BYTES;
   static constexpr int NBARS = 2 * kStages + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-  static constexpr int OFF_AMAX = OFF_MISC + 16;              // float [2 tiles][2 wg][128]
-  static constexpr int OFF_OFF = OFF_AMAX + 4 * 128 * 4;
+  static constexpr int OFF_AMAX = OFF_MISC + 16;  // float [2 tiles][kEpiGroups][128]
+  static constexpr int OFF_OFF = OFF_AMAX + 2 * kEpiGroups * 128 * 4;
   static constexpr int OFF_PREF = OFF_OFF + (kMaxE + 1) * 4;
   static constexpr int BYTES = OFF_PREF + (kMaxE + 1) * 4;
   static constexpr int SMEM = BYTES + 1024;
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 2) >> 2;  // warpgroup 0 or 1
+    const int wg = (warp - 2) >> 2;  // warpgroup 0..kEpiGroups-1
     const int q = warp & 3;          // TMEM lane quarter
     const int r = q * 32 + lane;
     const int KBn = p.K / 128;
@@ -258,22 +261,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m_e = s_off[e + 1] - s_off[e];
       const bool valid = m * BM + r < m_e;
       const long R = static_cast<long>(s_off[e]) + m * BM + r;
-      // weight block rows of this tile's columns
+      // weight block rows feeding this warpgroup's columns
       long wrow0, wrow1;
+      int col0, col1;  // partial-sum columns of acc0 / acc1
       if (EPI == EPI_SWIGLU_Q) {
         wrow0 = static_cast<long>(e) * (2 * p.I / 128) + n;              // gate block row
         wrow1 = static_cast<long>(e) * (2 * p.I / 128) + p.I / 128 + n;  // up block row
+        col0 = 32 * wg;
+        col1 = 128 + 32 * wg;
       } else {
-        wrow0 = static_cast<long>(e) * (p.H / 128) + 2 * n + wg;         // this warpgroup's block row
+        wrow0 = static_cast<long>(e) * (p.H / 128) + 2 * n + (kGroupCols * wg) / 128;
         wrow1 = wrow0;
+        col0 = kGroupCols * wg;
+        col1 = col0 + 32;
       }
-      float acc0[64], acc1[64];
+      float acc0[32], acc1[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
+      for (int i = 0; i < 32; ++i) acc0[i] = acc1[i] = 0.f;
       for (int kb = 0; kb < KB; ++kb, ++g) {
-        const float sa = valid ? load_scale(p.a_scale, static_cast<long>(kb) * p.n_rows + R, p.ue8m0) : 0.f;
+        const float sa =
+            valid ? load_scale(p.a_scale, static_cast<long>(kb) * p.n_rows + R, p.ue8m0) : 0.f;
         const float s0 = sa * load_scale(p.w_scale, wrow0 * KBn + kb, p.ue8m0);
-        const float s1 = sa * load_scale(p.w_scale, wrow1 * KBn + kb, p.ue8m0);
+        const float s1 =
+            (EPI == EPI_SWIGLU_Q) ? sa * load_scale(p.w_scale, wrow1 * KBn + kb, p.ue8m0) : s0;
         const int b = g & 1;
         int w_ok = 1;
         if (lane == 0)
@@ -286,50 +296,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
-        uint32_t v[32];
-        if (EPI == EPI_SWIGLU_Q) {
-          // gate columns 64wg.., up columns 128+64wg..
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_32x32b_x32(tb + 64 * wg + 32 * h, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc0[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc0[32 * h + i]);
-            tmem_ld_32x32b_x32(tb + 128 + 64 * wg + 32 * h, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc1[32 * h + i] = fmaf(__uint_as_float(v[i]), s1, acc1[32 * h + i]);
+        for (int h = 0; h < 4; ++h) {
+          uint32_t v0[8], v1[8];
+          tmem_ld_32x32b_x8(tb + col0 + 8 * h, v0);
+          tmem_ld_32x32b_x8(tb + col1 + 8 * h, v1);
+          tmem_ld_wait();
+          if (h == 3) {  // buffer fully read: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
           }
-        } else {
-          // output columns 128wg .. 128wg+127 -> acc0[0..63], acc1[0..63]
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_32x32b_x32(tb + 128 * wg + 32 * h, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc0[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc0[32 * h + i]);
-            tmem_ld_32x32b_x32(tb + 128 * wg + 64 + 32 * h, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc1[32 * h + i] = fmaf(__uint_as_float(v[i]), s0, acc1[32 * h + i]);
+          for (int i = 0; i < 8; ++i) {
+            acc0[8 * h + i] = fmaf(__uint_as_float(v0[i]), s0, acc0[8 * h + i]);
+            acc1[8 * h + i] = fmaf(__uint_as_float(v1[i]), s1, acc1[8 * h + i]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
       }
       if (!ok) break;
 
       if (EPI == EPI_SWIGLU_Q) {
-        // h = silu(g) * u over this warpgroup's 64 columns; the 1x128 block
-        // is the tile's 128 columns, shared with the other warpgroup.
+        // h = silu(g) * u over this warpgroup's 32 columns; the 1x128 block is
+        // the tile's 128 columns, shared by the four warpgroups.
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 32; ++i) {
           acc0[i] = silu_f(acc0[i]) * acc1[i];
           amax = fmaxf(amax, fabsf(acc0[i]));
         }
-        float* am = s_amax + (amax_phase ? 256 : 0);   // double-buffered by tile
+        float* am = s_amax + (amax_phase ? kEpiGroups * 128 : 0);   // double-buffered by tile
         am[wg * 128 + r] = amax;
         mbar_arrive(smem_u32(amax_bar));
         int a_ok = 1;
@@ -341,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        amax = fmaxf(am[r], am[128 + r]);
+        amax = am[r];
+#pragma unroll
+        for (int j = 1; j < kEpiGroups; ++j) amax = fmaxf(amax, am[j * 128 + r]);
         amax_phase ^= 1u;
         // scale as in the weight quantiser: amax/448 or its power-of-two ceiling
         float sc = 1.0f;
@@ -361,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float inv = 1.0f / sc;
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.hq + R * p.I + n * 128 + 64 * wg);
+          uint4* dst = reinterpret_cast<uint4*>(p.hq + R * p.I + n * 128 + 32 * wg);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 2; ++j) {
             uint32_t w4[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -383,15 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int f = __ldg(p.sorted_f + R);
           const int tok = f / p.k;
           const float wgt = __ldg(p.topk_w + f);
-          float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + 128 * wg;
+          float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + col0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < 8; ++j)
             atomicAdd(reinterpret_cast<float4*>(orow + 4 * j),
                       make_float4(wgt * acc0[4 * j], wgt * acc0[4 * j + 1], wgt * acc0[4 * j + 2],
                                   wgt * acc0[4 * j + 3]));
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            atomicAdd(reinterpret_cast<float4*>(orow + 64 + 4 * j),
+          for (int j = 0; j < 8; ++j)
+            atomicAdd(reinterpret_cast<float4*>(orow + 32 + 4 * j),
                       make_float4(wgt * acc1[4 * j], wgt * acc1[4 * j + 1], wgt * acc1[4 * j + 2],
                                   wgt * acc1[4 * j + 3]));
         }

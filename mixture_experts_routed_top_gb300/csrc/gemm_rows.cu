@@ -29,17 +29,22 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
-constexpr int kStages = 4;
+
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr int kBoxBytes = 128 * BK * 2;  // one 128-row TMA box
 
 enum { EPI_SWIGLU = 0, EPI_COMBINE = 1 };
 
-template <int BN>
+static_assert(kRowsBK == 64 || kRowsBK == 32, "K-block must be 64 or 32 bf16");
+
+// BK = bf16 elements per K-block: 64 (128-byte rows, 128-byte swizzle,
+// 4 stages of 48 KB) or 32 (64-byte rows, 64-byte swizzle, 9 stages of
+// 24 KB: the same shared memory holds more K-blocks in flight).
+template <int BN, int BK>
 struct Layout {
+  static constexpr int kStages = BK == 64 ? 4 : (BN == 256 ? 9 : 12);
+  static constexpr int kBoxBytes = 128 * BK * 2;  // one 128-row TMA box
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES;
@@ -80,11 +85,13 @@ __device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* 
   m = local - n * mt;
 }
 
-template <int EPI, int BN>
+template <int EPI, int BN, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_rows_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, const GemmDev p) {
-  using L = Layout<BN>;
+  using L = Layout<BN, BK>;
+  constexpr int kStages = L::kStages;
+  constexpr int kBoxBytes = L::kBoxBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -203,8 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_k_sw128(smem_u32(sA + stage * L::A_BYTES));
-          const uint64_t bd = sdesc_k_sw128(smem_u32(sB + stage * L::B_BYTES));
+          const uint32_t sa = smem_u32(sA + stage * L::A_BYTES);
+          const uint32_t sb = smem_u32(sB + stage * L::B_BYTES);
+          const uint64_t ad = BK == 64 ? sdesc_k_sw128(sa) : sdesc_k_sw64(sa);
+          const uint64_t bd = BK == 64 ? sdesc_k_sw128(sb) : sdesc_k_sw64(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -305,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int EPI, int BN>
 cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
-  using L = Layout<BN>;
-  auto kern = grouped_gemm_rows_kernel<EPI, BN>;
+  using L = Layout<BN, kRowsBK>;
+  auto kern = grouped_gemm_rows_kernel<EPI, BN, kRowsBK>;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;

@@ -122,18 +122,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major [outer, inner] matrix, box = box_rows rows x 128 bytes,
-// 128-byte swizzle, out-of-range rows read as zero.
+// 2-D row-major [outer, inner] matrix, box = box_rows rows x row_bytes
+// (128 or 64) bytes, swizzled at the same width, out-of-range rows read as
+// zero.
 moe_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
-                    uint64_t inner, uint64_t outer, uint32_t box_rows = 128) {
+                    uint64_t inner, uint64_t outer, uint32_t box_rows = 128,
+                    uint32_t row_bytes = 128) {
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * esize};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / esize), box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return MOE_OK;
@@ -169,20 +172,27 @@ struct Profiler {
 Profiler g_prof;
 std::mutex g_prof_mu;
 
+// Records a CUDA event pair around one stage of a forward.  Inside a stream
+// capture the events are recorded as external event nodes, so that after a
+// replay of the graph they hold that replay's times.
 struct StageScope {
   cudaStream_t s;
   int stage;
   cudaEvent_t b = nullptr;
+  unsigned flags = cudaEventRecordDefault;
   StageScope(cudaStream_t s_, int st) : s(s_), stage(st) {
     if (!g_prof.on) return;
     std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      flags = cudaEventRecordExternal;
     cudaEvent_t a = g_prof.get();
     b = g_prof.get();
-    cudaEventRecord(a, s);
+    cudaEventRecordWithFlags(a, s, flags);
     g_prof.recs.push_back({stage, a, b});
   }
   ~StageScope() {
-    if (b) cudaEventRecord(b, s);
+    if (b) cudaEventRecordWithFlags(b, s, flags);
   }
 };
 
@@ -346,6 +356,20 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     a.E = E;
     a.k = k;
     a.num_sms = sms;
+    if (n <= kFusedDecodeRows) {
+      // routing table rebuilt inside both kernels; the down kernel combines
+      {
+        StageScope sc(s, MOE_STAGE_GEMM1);
+        if ((e = launch_decode_fused_gate_up(a, topk_idx, d.err, s)) != cudaSuccess)
+          return cuda_fail(e, "decode_fused_gate_up");
+      }
+      {
+        StageScope sc(s, MOE_STAGE_GEMM2);
+        if ((e = launch_decode_fused_down(a, topk_idx, d.err, s)) != cudaSuccess)
+          return cuda_fail(e, "decode_fused_down");
+      }
+      return MOE_OK;
+    }
     {
       StageScope sc(s, MOE_STAGE_DISPATCH);
       if ((e = launch_dispatch_small(topk_idx, T, E, k, d, s)) != cudaSuccess)
@@ -445,19 +469,22 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
   const int swap_rows = moe_get_swap_rows();
   const bool swap1 = n <= static_cast<long>(swap_rows) * E;
   const bool swap2 = g_swap_rows >= 0 ? swap1 : true;
+  // swap-AB kernel: 128-byte rows, token boxes of 64 rows; token-row
+  // kernel: rows of kRowsBK bf16, 128-row boxes for both operands
+  const uint32_t rb = kRowsBK * 2;
   CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
   moe_status st;
-  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, swap1 ? 64 : 128)) !=
-      MOE_OK)
+  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, swap1 ? 64 : 128,
+                     swap1 ? 128 : rb)) != MOE_OK)
     return st;
   if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
-                     static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+                     static_cast<uint64_t>(E) * 2 * I, 128, swap1 ? 128 : rb)) != MOE_OK)
     return st;
-  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, swap2 ? 64 : 128)) !=
-      MOE_OK)
+  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, swap2 ? 64 : 128,
+                     swap2 ? 128 : rb)) != MOE_OK)
     return st;
   if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
-                     static_cast<uint64_t>(E) * H)) != MOE_OK)
+                     static_cast<uint64_t>(E) * H, 128, swap2 ? 128 : rb)) != MOE_OK)
     return st;
 
   {
@@ -576,6 +603,7 @@ int moe_profile_end(float* stage_ms, int* stage_launches, int n) {
     g_prof.pool.push_back(r.b);
   }
   g_prof.recs.clear();
+  (void)cudaGetLastError();  // a pair that could not be timed leaves no pending error behind
   for (int i = 0; i < n && i < MOE_STAGE_COUNT; ++i) {
     if (stage_ms) stage_ms[i] = ms[i];
     if (stage_launches) stage_launches[i] = cnt[i];

@@ -96,6 +96,7 @@ cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm1_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
 
 // FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
@@ -134,12 +135,17 @@ struct DecodeArgs {
   void* out;                 // bf16 [T, H]
   int T, H, I, E, k, num_sms;
 };
-constexpr int kDecodeRowsDefault = 16;    // T*k at or below: decode path (measured crossover)
+constexpr int kDecodeRowsDefault = 8;     // T*k at or below: decode path (measured crossover)
 constexpr int kDecodeRowsMax = 2048;      // the decode path's workspace is sized up to this
+constexpr int kFusedDecodeRows = 64;      // T*k at or below: two fused decode kernels
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
                                   const DispatchBufs& d, cudaStream_t s);
 cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk_idx, int* err,
+                                       cudaStream_t s);
+cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_idx, int* err,
+                                     cudaStream_t s);
 
 }  // namespace moe
