@@ -142,6 +142,26 @@ class ClockSampler:
                 "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "nvml"}
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over all ranks (identity without a process group).
+    Each rank runs an independent replica; the job's time is the slowest."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank processed its own batch of
+    tokens_per_step in each of the steps; the job took the slowest rank's
+    max_ms milliseconds."""
+    return world * tokens_per_step * steps / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------ workload
 def build_workload(name, device):
     import torch
@@ -359,11 +379,7 @@ def run_ours(args, rank, world, local_rank):
     stages = moe.profile_end()
     launches = (per_step_launches * args.steps) if graph is not None else moe.launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     moe.workspace_status(ws)
 
     # ---------------------------------------------------------- end to end
@@ -391,18 +407,14 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     if not torch.equal(o_host, out.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident run")
 
     # ---------------------------------------------------------- report
     peaks, peak_src = load_peaks()
     ms_per_step = total_ms / args.steps
-    tok_s = world * s.T * args.steps / (total_ms / 1e3)
+    tok_s = job_throughput(s.T, args.steps, world, total_ms)
     g1_ms, g1_n = stages["gemm1"]
     g2_ms, g2_n = stages["gemm2"]
     bytes_per_w = 1.0 if w["wfmt"] == "fp8" else 2.0
@@ -427,7 +439,7 @@ def run_ours(args, rank, world, local_rank):
                  "peak_source": f"{peak_src} ({'bf16 burst' if w['wfmt'] == 'bf16' else 'bf16 burst x2 nominal fp8/bf16 ratio'})",
                  "algorithmic_per_launch": {"flops": kern_flops, "weight_bytes": kern_wbytes},
                  "avg_launch_ms": round(d_avg_s * 1e3, 4)})
-    e2e_tok_s = world * s.T * args.steps / (e2e_ms / 1e3)
+    e2e_tok_s = job_throughput(s.T, args.steps, world, e2e_ms)
     line = {
         "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
