@@ -67,11 +67,11 @@ struct Fp8Dev {
   const int* tile_pref;
   int E, K, I, H, k, n_rows;
   int* err;
-  const void* a_scale;  // [K/128, n_rows], fp32 or UE8M0 byte
+  const void* a_scale;  // [n_rows, scale_stride(K/128)], fp32 or UE8M0 byte
   const void* w_scale;  // [E, Nw/128, K/128], fp32 or UE8M0 byte
   int ue8m0;
   uint8_t* hq;          // gate/up: h codes [n_rows, I]
-  void* hs;             // gate/up: h scales [I/128, n_rows]
+  void* hs;             // gate/up: h scales [n_rows, scale_stride(I/128)]
   float* out32;         // down: [T, H]
   const int* sorted_f;
   const float* topk_w;
@@ -278,41 +278,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc0[32], acc1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc0[i] = acc1[i] = 0.f;
-      for (int kb = 0; kb < KB; ++kb, ++g) {
-        const float sa =
-            valid ? load_scale(p.a_scale, static_cast<long>(kb) * p.n_rows + R, p.ue8m0) : 0.f;
-        const float s0 = sa * load_scale(p.w_scale, wrow0 * KBn + kb, p.ue8m0);
-        const float s1 =
-            (EPI == EPI_SWIGLU_Q) ? sa * load_scale(p.w_scale, wrow1 * KBn + kb, p.ue8m0) : s0;
-        const int b = g & 1;
-        int w_ok = 1;
-        if (lane == 0)
-          w_ok = mbar_wait_bounded(smem_u32(&pfull[b]), (g >> 1) & 1, s_abort, p.err,
-                                   ERR_TIMEOUT_EPILOGUE);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
+      // Scales of K-blocks kb0..kb0+3: the row's activation scales with one
+      // vector load, the tile's weight-block scales by lanes 0-7 of the warp
+      // (broadcast by shuffle); loaded one group ahead of their use.
+      const int sstride = scale_stride(KBn);
+      const long arow_base = R * sstride;
+      auto load_group = [&](int kb0, float (&sa4)[4], float& wl) {
+        sa4[0] = sa4[1] = sa4[2] = sa4[3] = 0.f;
+        wl = 0.f;
+        if (kb0 >= KB) return;
+        if (valid) {
+          if (p.ue8m0) {
+            const uint32_t b4 = __ldg(reinterpret_cast<const uint32_t*>(
+                static_cast<const uint8_t*>(p.a_scale) + arow_base + kb0));
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t v0[8], v1[8];
-          tmem_ld_32x32b_x8(tb + col0 + 8 * h, v0);
-          tmem_ld_32x32b_x8(tb + col1 + 8 * h, v1);
-          tmem_ld_wait();
-          if (h == 3) {  // buffer fully read: the MMA may reuse it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc0[8 * h + i] = fmaf(__uint_as_float(v0[i]), s0, acc0[8 * h + i]);
-            acc1[8 * h + i] = fmaf(__uint_as_float(v1[i]), s1, acc1[8 * h + i]);
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t bb = (b4 >> (8 * u)) & 0xFFu;
+              sa4[u] = bb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(bb << 23);
+            }
+          } else {
+            const float4 f4 = __ldg(reinterpret_cast<const float4*>(
+                static_cast<const float*>(p.a_scale) + arow_base + kb0));
+            sa4[0] = f4.x;
+            sa4[1] = f4.y;
+            sa4[2] = f4.z;
+            sa4[3] = f4.w;
           }
         }
+        const int u = lane & 3;
+        if (lane < 8 && kb0 + u < KB)
+          wl = load_scale(p.w_scale, (lane < 4 ? wrow0 : wrow1) * KBn + kb0 + u, p.ue8m0);
+      };
+      float sa_c[4], sa_n[4], w_c, w_n;
+      load_group(0, sa_c, w_c);
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
+        load_group(kb0 + 4, sa_n, w_n);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float sw0 = __shfl_sync(0xffffffffu, w_c, u);
+          const float sw1 = __shfl_sync(0xffffffffu, w_c, 4 + u);
+          if (kb0 + u >= KB) break;
+          const float s0 = sa_c[u] * sw0;
+          const float s1 = (EPI == EPI_SWIGLU_Q) ? sa_c[u] * sw1 : s0;
+          const int b = g & 1;
+          int w_ok = 1;
+          if (lane == 0)
+            w_ok = mbar_wait_bounded(smem_u32(&pfull[b]), (g >> 1) & 1, s_abort, p.err,
+                                     ERR_TIMEOUT_EPILOGUE);
+          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          if (!w_ok) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint32_t v0[8], v1[8];
+            tmem_ld_32x32b_x8(tb + col0 + 8 * h, v0);
+            tmem_ld_32x32b_x8(tb + col1 + 8 * h, v1);
+            tmem_ld_wait();
+            if (h == 3) {  // buffer fully read: the MMA may reuse it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc0[8 * h + i] = fmaf(__uint_as_float(v0[i]), s0, acc0[8 * h + i]);
+              acc1[8 * h + i] = fmaf(__uint_as_float(v1[i]), s1, acc1[8 * h + i]);
+            }
+          }
+          ++g;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sa_c[u] = sa_n[u];
+        w_c = w_n;
       }
       if (!ok) break;
 
@@ -371,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
           if (wg == 0) {
-            const long si = static_cast<long>(n) * p.n_rows + R;
+            const long si = R * scale_stride(p.I / 128) + n;
             if (p.ue8m0) static_cast<uint8_t*>(p.hs)[si] = static_cast<uint8_t>(stored);
             else static_cast<uint32_t*>(p.hs)[si] = stored;
           }

@@ -88,9 +88,9 @@ WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
   L.blk_counts = take(nchunks * E * 4);
   const size_t esz = fp8 ? 1 : 2;
   L.xa = take(n * H * esz);
-  L.xa_scale = take(fp8 ? n * (H / 128) * 4 : 0);
+  L.xa_scale = take(fp8 ? n * scale_stride(H / 128) * 4 : 0);
   L.hb = take(n * I * esz);
-  L.hb_scale = take(fp8 ? n * (I / 128) * 4 : 0);
+  L.hb_scale = take(fp8 ? n * scale_stride(I / 128) * 4 : 0);
   L.out32 = take(T * H * 4);
   L.ydec = take(n <= kDecodeRowsMax ? n * H * 4 : 0);
   L.total = align_up(off, 1024);

@@ -54,6 +54,10 @@ moe_status set_last_error(moe_status st, const char* fmt, ...);
 // Counts every kernel launch the library makes (exported as moe_launch_count).
 void count_launches(int n);
 
+// Row stride (in scale entries) of the per-row 1x128 activation scales:
+// the block count rounded up to a multiple of 4.
+__host__ __device__ inline int scale_stride(int nblocks) { return (nblocks + 3) & ~3; }
+
 inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); }
 
 // Kernel launchers (return cudaGetLastError()).
@@ -107,11 +111,11 @@ struct GroupedGemmFp8Args {
   const int* tile_pref;
   int E, K, I, H, k, n_rows;
   int* err;
-  const void* a_scale;       // [K/128, n_rows]
+  const void* a_scale;       // [n_rows, scale_stride(K/128)]
   const void* w_scale;       // [E, Nw/128, K/128]
   bool ue8m0;
   void* hq;                  // gate/up output codes [n_rows, I]
-  void* hs;                  // gate/up output scales [I/128, n_rows]
+  void* hs;                  // gate/up output scales [n_rows, scale_stride(I/128)]
   float* out32;              // down output accumulator [T, H]
   const int* sorted_f;
   const float* topk_w;

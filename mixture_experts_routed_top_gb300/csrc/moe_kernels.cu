@@ -272,38 +272,62 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Gather + dynamic 1x128 activation quantisation: one warp per row, each
-// lane owns 4 consecutive elements of every 128-wide block.  Codes go to
-// xq[r, :], scales to xs[b, r] (K-block major, so that the GEMM epilogue's
-// per-row scale reads are coalesced).
-__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint2* __restrict__ hidden, int H,
+// Gather + dynamic 1x128 activation quantisation: one warp per row; each
+// half-warp quantises one 128-wide block (16 lanes x 8 elements), and a lane
+// issues the loads of four blocks (eight per warp) before any arithmetic.
+// Codes go to xq[r, :], scales to xs[r, b] with a row stride of
+// scale_stride(H/128) blocks (a multiple of 4, so that one vector load
+// fetches four blocks' scales).
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ hidden, int H,
                                                          int k, const int* __restrict__ sorted_f,
                                                          const int* __restrict__ nvalid, int rows,
-                                                         bool ue8m0, uint32_t* __restrict__ xq,
+                                                         bool ue8m0, uint2* __restrict__ xq,
                                                          void* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, l16 = lane & 15;
   const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (r >= rows || r >= *nvalid) return;
   const long t = __ldg(sorted_f + r) / k;
   const int nb = H / 128;
-  const uint2* src = hidden + t * (H / 4);
-  uint32_t* dst = xq + r * (H / 4);
-  for (int b = 0; b < nb; ++b) {
-    const uint2 raw = __ldg(src + b * 32 + lane);
-    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    const float x0 = __low2float(p0), x1 = __high2float(p0);
-    const float x2 = __low2float(p1), x3 = __high2float(p1);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
-    uint32_t stored;
-    const float sc = block_scale(amax, ue8m0, &stored);
-    const float inv = 1.0f / sc;
-    const uint32_t lo = e4m3x2(x0 * inv, x1 * inv);
-    const uint32_t hi = e4m3x2(x2 * inv, x3 * inv);
-    dst[b * 32 + lane] = lo | (hi << 16);
-    if (lane == 0) {  // scales are K-block major: xs[b][r]
-      if (ue8m0) static_cast<uint8_t*>(xs)[static_cast<long>(b) * rows + r] = static_cast<uint8_t>(stored);
-      else static_cast<uint32_t*>(xs)[static_cast<long>(b) * rows + r] = stored;
+  const long sstride = scale_stride(nb);
+  const uint4* src = hidden + t * (H / 8);
+  uint2* dst = xq + r * (H / 8);
+  for (int b0 = 0; b0 < nb; b0 += 8) {
+    uint4 raw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int b = b0 + 2 * i + half;
+      raw[i] = b < nb ? __ldg(src + b * 16 + l16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int b = b0 + 2 * i + half;
+      float x[8];
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)  // stays inside the half-warp
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      uint32_t stored;
+      const float sc = block_scale(amax, ue8m0, &stored);
+      const float inv = 1.0f / sc;
+      if (b < nb) {
+        const uint32_t c0 = e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16);
+        const uint32_t c1 = e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16);
+        dst[b * 16 + l16] = make_uint2(c0, c1);
+        if (l16 == 0) {
+          const long si = r * sstride + b;
+          if (ue8m0) static_cast<uint8_t*>(xs)[si] = static_cast<uint8_t>(stored);
+          else static_cast<uint32_t*>(xs)[si] = stored;
+        }
+      }
     }
   }
 }
@@ -312,9 +336,9 @@ cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorte
                               const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
                               cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  gather_fp8_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint2*>(hidden), H, k,
+  gather_fp8_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4*>(hidden), H, k,
                                                       sorted_f, nvalid, rows, ue8m0,
-                                                      reinterpret_cast<uint32_t*>(xq), xs);
+                                                      reinterpret_cast<uint2*>(xq), xs);
   count_launches(1);
   return cudaGetLastError();
 }
