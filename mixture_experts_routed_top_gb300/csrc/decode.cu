@@ -101,45 +101,36 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8], 
 constexpr int kStreamBatch = 8;  // 16-byte weight vectors per lane loaded before any math
 
 // ag[t] += w_gate . x_t and au[t] += w_up . x_t over 16-byte vectors
-// lane, lane+32, ... < n8 of two weight rows; each lane first issues
-// kStreamBatch loads per row, then does the arithmetic.
+// lane, lane+32, ... < n8 of two weight rows; each lane first issues up to
+// kStreamBatch loads per row (the tail of a short row included, guarded),
+// then does the arithmetic.
 template <int MT>
 __device__ __forceinline__ void stream_dot2(const uint4* __restrict__ wg,
                                             const uint4* __restrict__ wu,
                                             const uint4* const (&xr)[MT], int n8, int lane,
                                             float (&ag)[MT], float (&au)[MT]) {
-  int c0 = lane;
-  for (; c0 + 32 * (kStreamBatch - 1) < n8; c0 += 32 * kStreamBatch) {
+  for (int c0 = lane; c0 < n8; c0 += 32 * kStreamBatch) {
     uint4 g[kStreamBatch], u[kStreamBatch];
 #pragma unroll
     for (int i = 0; i < kStreamBatch; ++i) {
-      g[i] = ld_stream(wg + c0 + 32 * i);
-      u[i] = ld_stream(wu + c0 + 32 * i);
+      const int c = c0 + 32 * i;
+      g[i] = c < n8 ? ld_stream(wg + c) : make_uint4(0, 0, 0, 0);
+      u[i] = c < n8 ? ld_stream(wu + c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kStreamBatch; ++i) {
+      const int c = c0 + 32 * i;
+      if (c >= n8) break;
       float gf[8], uf[8];
       bf16x8_to_f32(g[i], gf);
       bf16x8_to_f32(u[i], uf);
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         float xf[8];
-        bf16x8_to_f32(__ldg(xr[t] + c0 + 32 * i), xf);
+        bf16x8_to_f32(__ldg(xr[t] + c), xf);
         ag[t] = dot8(gf, xf, ag[t]);
         au[t] = dot8(uf, xf, au[t]);
       }
-    }
-  }
-  for (; c0 < n8; c0 += 32) {
-    float gf[8], uf[8];
-    bf16x8_to_f32(ld_stream(wg + c0), gf);
-    bf16x8_to_f32(ld_stream(wu + c0), uf);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      float xf[8];
-      bf16x8_to_f32(__ldg(xr[t] + c0), xf);
-      ag[t] = dot8(gf, xf, ag[t]);
-      au[t] = dot8(uf, xf, au[t]);
     }
   }
 }
@@ -149,31 +140,25 @@ template <int MT>
 __device__ __forceinline__ void stream_dot1(const uint4* __restrict__ w,
                                             const uint4* const (&xr)[MT], int n8, int lane,
                                             float (&acc)[MT]) {
-  int c0 = lane;
-  for (; c0 + 32 * (kStreamBatch - 1) < n8; c0 += 32 * kStreamBatch) {
+  for (int c0 = lane; c0 < n8; c0 += 32 * kStreamBatch) {
     uint4 v[kStreamBatch];
 #pragma unroll
-    for (int i = 0; i < kStreamBatch; ++i) v[i] = ld_stream(w + c0 + 32 * i);
+    for (int i = 0; i < kStreamBatch; ++i) {
+      const int c = c0 + 32 * i;
+      v[i] = c < n8 ? ld_stream(w + c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int i = 0; i < kStreamBatch; ++i) {
+      const int c = c0 + 32 * i;
+      if (c >= n8) break;
       float wf[8];
       bf16x8_to_f32(v[i], wf);
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         float xf[8];
-        bf16x8_to_f32(__ldg(xr[t] + c0 + 32 * i), xf);
+        bf16x8_to_f32(__ldg(xr[t] + c), xf);
         acc[t] = dot8(wf, xf, acc[t]);
       }
-    }
-  }
-  for (; c0 < n8; c0 += 32) {
-    float wf[8];
-    bf16x8_to_f32(ld_stream(w + c0), wf);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      float xf[8];
-      bf16x8_to_f32(__ldg(xr[t] + c0), xf);
-      acc[t] = dot8(wf, xf, acc[t]);
     }
   }
 }

@@ -139,7 +139,7 @@ struct DecodeArgs {
   void* out;                 // bf16 [T, H]
   int T, H, I, E, k, num_sms;
 };
-constexpr int kDecodeRowsDefault = 8;     // T*k at or below: decode path (measured crossover)
+constexpr int kDecodeRowsDefault = 16;    // T*k at or below: decode path (measured crossover)
 constexpr int kDecodeRowsMax = 2048;      // the decode path's workspace is sized up to this
 constexpr int kFusedDecodeRows = 64;      // T*k at or below: two fused decode kernels
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
