@@ -49,12 +49,16 @@ WORKLOADS = {
     "dsv3-fp8-64-ue8m0": ("dsv3_fp8", 64, "fp8", "ue8m0"),
     "dsv3-fp8-16384-f32": ("dsv3_fp8", 16384, "fp8", "f32"),
     "dsv3-fp8-16384-ue8m0": ("dsv3_fp8", 16384, "fp8", "ue8m0"),
+    # profiling-sized layers (32 experts), used for ncu captures
+    "dsv3e32-fp8-2048-f32": ("dsv3_e32", 2048, "fp8", "f32"),
+    "dsv3e32-fp8-8-f32": ("dsv3_e32", 8, "fp8", "f32"),
 }
 DESCRIPTIONS = {
     "qwen": "Qwen1.5-MoE-A2.7B-shaped MoE layer",
     "tiny": "tiny MoE FFN",
     "dsv3": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) expert skew",
     "dsv3_fp8": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) skew, e4m3 128x128 block-scaled weights",
+    "dsv3_e32": "DeepSeek-V3-width MoE layer with 32 experts (profiling size), e4m3 weights",
 }
 L2_BYTES = 129 * 2 ** 20
 

@@ -14,6 +14,8 @@ Workload shapes (the layer sizes of the benchmark cases):
                router logits skewed by a Zipf(s=1.1) expert bias
 * ``dsv3_fp8`` - the DeepSeek-V3 shape with block-scaled e4m3 weights,
                T in {64, 16384}
+* ``dsv3_e32`` - the DeepSeek-V3 width with 32 experts, uniform routing
+               (profiling-sized)
 
 Value recipe: hidden ~ N(0,1) rounded to bf16, expert weights ~ N(0, 0.02^2)
 rounded to bf16, router logits ~ N(0,1) in fp32.  For the skewed workloads a
@@ -56,6 +58,9 @@ SHAPES = {
     "qwen": MoEShape(T=4096, H=2048, I=1408, E=60, k=4),
     "dsv3": MoEShape(T=8192, H=7168, I=2048, E=256, k=8, zipf_s=1.1),
     "dsv3_fp8": MoEShape(T=16384, H=7168, I=2048, E=256, k=8, zipf_s=1.1),
+    # DeepSeek-V3 width with 32 experts and uniform routing: a layer small
+    # enough (1.4 GB of e4m3 weights) for detailed profiler captures
+    "dsv3_e32": MoEShape(T=2048, H=7168, I=2048, E=32, k=8),
 }
 
 
