@@ -438,9 +438,11 @@ def run_ours(args, rank, world, local_rank):
         achieved = kern_flops / d_avg_s / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
                 "unit": "TFLOP/s", "frac": round(achieved / pk, 4)}
+    peak_kind = ("hbm_gbs, STREAM-style copy" if hbm_bound else
+                 "bf16 burst" if w["wfmt"] == "bf16" else "bf16 burst x2 nominal fp8/bf16 ratio")
     kernel_key = f"{dominant}:{args.workload}"
     roof.update({"traffic": traffic_for(kernel_key), "kernel": dominant,
-                 "peak_source": f"{peak_src} ({'bf16 burst' if w['wfmt'] == 'bf16' else 'bf16 burst x2 nominal fp8/bf16 ratio'})",
+                 "peak_source": f"{peak_src} ({peak_kind})",
                  "algorithmic_per_launch": {"flops": kern_flops, "weight_bytes": kern_wbytes},
                  "avg_launch_ms": round(d_avg_s * 1e3, 4)})
     e2e_tok_s = job_throughput(s.T, args.steps, world, e2e_ms)
