@@ -343,47 +343,70 @@ def run_ours(args, rank, world, local_rank):
         step(w["logits"], w["hidden"])
     torch.cuda.synchronize()
 
-    graph = None
+    graph = graph_prof = None
     if args.graph:
-        # One step captured as a CUDA graph (router + forward, all kernels of
-        # the library); the per-stage CUDA events are captured with it.
-        moe.profile_begin()
+        # One step (router + forward, every kernel of the library) captured
+        # as a CUDA graph for the timed region, and a second capture of the
+        # same step with per-stage CUDA events for the per-kernel durations:
+        # the event nodes add several microseconds per stage, so they stay
+        # out of the timed steps.
         n_cap = moe.launch_count()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step(w["logits"], w["hidden"])
         per_step_launches = moe.launch_count() - n_cap
+        moe.profile_begin()
+        graph_prof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_prof):
+            step(w["logits"], w["hidden"])
         for _ in range(args.warmup):
             graph.replay()
+            graph_prof.replay()
         torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    n0 = moe.launch_count()
-    if graph is None:
-        moe.profile_begin()
-    with ClockSampler(dev.index) as clk:
+    def timed_steps(profiled):
+        """K steps with the L2 flush between them; per-step CUDA events on the
+        launching stream. With profiled=True the stage events are on too and
+        their sums are returned."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        acc = {}
+        if profiled and graph is None:
+            moe.profile_begin()
         for i in range(args.steps):
             if flush:
                 flush_buf.zero_()
             starts[i].record(stream)
             if graph is not None:
-                graph.replay()
+                (graph_prof if profiled else graph).replay()
             else:
                 step(w["logits"], w["hidden"])
             ends[i].record(stream)
+            if profiled and graph is not None:
+                torch.cuda.synchronize()
+                for k_, (ms_, n_) in moe.profile_read().items():
+                    a_ = acc.get(k_, (0.0, 0))
+                    acc[k_] = (a_[0] + ms_, a_[1] + n_)
         torch.cuda.synchronize()
+        if profiled:
+            ended = moe.profile_end()
+            if graph is None:
+                acc = ended
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)], acc
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # with a graph the captured stage events hold the last replay's times
-    stages = moe.profile_end()
+    n0 = moe.launch_count()
+    with ClockSampler(dev.index) as clk:
+        step_ms, _ = timed_steps(profiled=False)
     launches = (per_step_launches * args.steps) if graph is not None else moe.launch_count() - n0
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     total_ms = max_over_ranks(sum(step_ms), dev)
+    # per-stage kernel durations: the same K steps again, with stage events
+    _, stages = timed_steps(profiled=True)
     moe.workspace_status(ws)
 
     # ---------------------------------------------------------- end to end
@@ -460,6 +483,10 @@ def run_ours(args, rank, world, local_rank):
                    "bf16_gemm": args.bf16_gemm,
                    "timed_steps": "CUDA graph replays of one captured step" if args.graph
                                   else "steps launched from Python",
+                   "stage_timing": ("per-stage CUDA events in a second capture of the same "
+                                    "step, replayed K times after the timed region")
+                                   if args.graph else
+                                   "per-stage CUDA events in K more steps after the timed region",
                    "workspace_bytes": ws_bytes},
         "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
         "weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),

@@ -201,6 +201,15 @@ moe_status moe_profile_begin(void);
 int moe_profile_end(float* stage_ms, int* stage_launches, int n);
 
 /*
+ * moe_profile_read - the same report as moe_profile_end() without ending the
+ * session or releasing its events.  Meant for forwards captured in a CUDA
+ * graph while profiling was on: every replay re-records the captured event
+ * pairs, so reading after each replay gives that replay's stage times.
+ * Synchronises the events; returns the number of stages.  Not thread-safe.
+ */
+int moe_profile_read(float* stage_ms, int* stage_launches, int n);
+
+/*
  * moe_dispatch_noalloc - moe_dispatch for callers that cannot allocate
  * device memory.  The page has no counterpart to this entry point; it exists
  * for integration only.

@@ -19,7 +19,8 @@ from . import build as _build
 __all__ = [
     "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
     "experts_forward", "quantize_fp8_blocks", "workspace_status", "set_decode_rows",
-    "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "selftest_wait_timeout", "launch_count",
+    "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
+    "selftest_wait_timeout", "launch_count",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0",
 ]
@@ -58,6 +59,7 @@ _SIGS = {
     "moe_get_swap_rows": ([], _I),
     "moe_profile_begin": ([], _I),
     "moe_profile_end": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
+    "moe_profile_read": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
     "moe_selftest_wait_timeout": ([_P, _SZ, _I, _P], _I),
     "moe_launch_count": ([], ctypes.c_longlong),
 }
@@ -267,6 +269,16 @@ def profile_end():
     ms = (ctypes.c_float * n)()
     cnt = (ctypes.c_int * n)()
     lib().moe_profile_end(ms, cnt, n)
+    return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def profile_read():
+    """-> {stage: (total_ms, launches)} of the forwards recorded so far, without
+    ending the session (after a CUDA-graph replay: that replay's times)."""
+    n = len(STAGES)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    lib().moe_profile_read(ms, cnt, n)
     return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
 
 

@@ -508,4 +508,8 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+bool decode_fused_fits(const DecodeArgs& a) {
+  return static_cast<long>(a.T) * a.k <= kFusedDecodeRows;
+}
+
 }  // namespace moe

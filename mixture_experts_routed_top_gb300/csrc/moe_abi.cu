@@ -356,7 +356,7 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     a.E = E;
     a.k = k;
     a.num_sms = sms;
-    if (n <= kFusedDecodeRows) {
+    if (decode_fused_fits(a)) {
       // routing table rebuilt inside both kernels; the down kernel combines
       {
         StageScope sc(s, MOE_STAGE_GEMM1);
@@ -587,9 +587,8 @@ moe_status moe_profile_begin(void) {
   return MOE_OK;
 }
 
-int moe_profile_end(float* stage_ms, int* stage_launches, int n) {
-  std::lock_guard<std::mutex> g(g_prof_mu);
-  g_prof.on = false;
+// Sums the elapsed time of every recorded pair per stage (caller holds the lock).
+static void profile_collect(float* stage_ms, int* stage_launches, int n) {
   std::vector<float> ms(MOE_STAGE_COUNT, 0.f);
   std::vector<int> cnt(MOE_STAGE_COUNT, 0);
   for (auto& r : g_prof.recs) {
@@ -599,15 +598,29 @@ int moe_profile_end(float* stage_ms, int* stage_launches, int n) {
       ms[r.stage] += t;
       cnt[r.stage] += 1;
     }
-    g_prof.pool.push_back(r.a);
-    g_prof.pool.push_back(r.b);
   }
-  g_prof.recs.clear();
   (void)cudaGetLastError();  // a pair that could not be timed leaves no pending error behind
   for (int i = 0; i < n && i < MOE_STAGE_COUNT; ++i) {
     if (stage_ms) stage_ms[i] = ms[i];
     if (stage_launches) stage_launches[i] = cnt[i];
   }
+}
+
+int moe_profile_end(float* stage_ms, int* stage_launches, int n) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof.on = false;
+  profile_collect(stage_ms, stage_launches, n);
+  for (auto& r : g_prof.recs) {
+    g_prof.pool.push_back(r.a);
+    g_prof.pool.push_back(r.b);
+  }
+  g_prof.recs.clear();
+  return MOE_STAGE_COUNT;
+}
+
+int moe_profile_read(float* stage_ms, int* stage_launches, int n) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  profile_collect(stage_ms, stage_launches, n);
   return MOE_STAGE_COUNT;
 }
 

@@ -147,6 +147,8 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
+// True when the two fused decode kernels apply (T*k <= kFusedDecodeRows).
+bool decode_fused_fits(const DecodeArgs& a);
 cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk_idx, int* err,
                                        cudaStream_t s);
 cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_idx, int* err,

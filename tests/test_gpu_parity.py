@@ -159,6 +159,23 @@ def test_forward_bf16_one_expert_takes_all(moe, path):
     assert O.rel_max_err(out, ref) <= BF16_TOL
 
 
+@pytest.mark.parametrize("path", ["decode"], indirect=True)
+@pytest.mark.parametrize("shape", [
+    MoEShape(T=2, H=7168, I=256, E=8, k=8),        # DeepSeek-V3 width, every expert touched
+    MoEShape(T=16, H=256, I=128, E=4, k=1),        # several tokens per expert
+    MoEShape(T=16, H=128, I=256, E=1, k=1),        # 16 tokens on one expert: 2 token chunks
+    MoEShape(T=4, H=2048, I=1408, E=60, k=4),      # Qwen width at the default threshold
+])
+def test_forward_bf16_fused_decode(moe, shape, path):
+    """Few routed rows: the two fused decode kernels run (two launches, no
+    dispatch or combine kernel), including the widest rows and the most
+    tokens per expert they see."""
+    n0 = moe.launch_count()
+    out, ref = _forward_case(moe, shape)
+    assert moe.launch_count() - n0 == 2
+    assert O.rel_max_err(out, ref) <= BF16_TOL
+
+
 def test_all_paths_agree(moe):
     shape = MoEShape(T=96, H=512, I=384, E=16, k=4)
     d = make_inputs(shape, seed=5, device="cuda")
