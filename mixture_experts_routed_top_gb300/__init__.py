@@ -197,7 +197,9 @@ def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.
     nbytes = workspace_size(T, H, I, E, k, wdtype)
     if workspace is None:
         key = hidden.device
-        workspace = _DEFAULT_WS.setdefault(key, Workspace(key))
+        workspace = _DEFAULT_WS.get(key)
+        if workspace is None:
+            workspace = _DEFAULT_WS.setdefault(key, Workspace(key))
     ws = workspace.get(nbytes)
     _check(lib().moe_experts_forward(
         _ptr(hidden), T, H, _ptr(topk_idx), _ptr(topk_w), E, k, I, _ptr(w_gate_up),
