@@ -23,6 +23,8 @@ namespace moe {
 __global__ void __launch_bounds__(1024) dispatch_small_kernel(
     const int32_t* __restrict__ idx, int n, int E, int* counts, int* offsets, int* tile_pref,
     int* touched, int* sorted_f, int* row_of, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_cur[kMaxE];
   __shared__ int s_warp[33];
@@ -176,6 +178,8 @@ __global__ void __launch_bounds__(128) decode_gate_up_kernel(
     const __nv_bfloat16* __restrict__ wgu, const int* __restrict__ offsets,
     const int* __restrict__ touched, const int* __restrict__ sorted_f,
     __nv_bfloat16* __restrict__ h_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_e = I / 4;
   const long n_items = static_cast<long>(__ldg(touched)) * per_e;
@@ -216,6 +220,8 @@ __global__ void __launch_bounds__(128) decode_down_kernel(
     const __nv_bfloat16* __restrict__ h, int H, int I, const __nv_bfloat16* __restrict__ wd,
     const int* __restrict__ offsets, const int* __restrict__ touched,
     const int* __restrict__ sorted_f, const float* __restrict__ topk_w, float* __restrict__ Y) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_e = H / 4;
   const long n_items = static_cast<long>(__ldg(touched)) * per_e;
@@ -252,6 +258,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __res
                                                              const int* __restrict__ row_of,
                                                              int T, int H, int k,
                                                              uint2* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int H4 = H / 4;
   const long total = static_cast<long>(T) * H4;
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -329,6 +337,8 @@ __global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
     const __nv_bfloat16* __restrict__ hidden, int H, int I, int k, int E, int n,
     const __nv_bfloat16* __restrict__ wgu, const int32_t* __restrict__ topk_idx,
     __nv_bfloat16* __restrict__ h_out, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ SmallTable tab;
   build_small_table(topk_idx, n, E, tab, err);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -373,6 +383,8 @@ __global__ void __launch_bounds__(128) decode_fused_down_kernel(
     const __nv_bfloat16* __restrict__ h, int T, int H, int I, int k, int E, int n,
     const __nv_bfloat16* __restrict__ wd, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ topk_w, __nv_bfloat16* __restrict__ out, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ SmallTable tab;
   __shared__ float s_acc[4][kFusedDecodeRows];
   build_small_table(topk_idx, n, E, tab, err);
@@ -417,7 +429,7 @@ __global__ void __launch_bounds__(128) decode_fused_down_kernel(
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
                                   const DispatchBufs& d, cudaStream_t s) {
   const int n = T * k;
-  dispatch_small_kernel<<<1, 1024, 0, s>>>(topk_idx, n, E, d.counts, d.offsets, d.tile_pref,
+  launch_pdl(dispatch_small_kernel, 1, 1024, 0, s, topk_idx, n, E, d.counts, d.offsets, d.tile_pref,
                                            d.touched, d.sorted_f, d.row_of, d.err);
   count_launches(1);
   return cudaGetLastError();
@@ -438,10 +450,10 @@ cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s) {
   auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   switch (mt_for(a.T)) {
-    case 8: decode_gate_up_kernel<8><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    case 4: decode_gate_up_kernel<4><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    case 2: decode_gate_up_kernel<2><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    default: decode_gate_up_kernel<1><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 8: launch_pdl(decode_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 4: launch_pdl(decode_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 2: launch_pdl(decode_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    default: launch_pdl(decode_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
   }
   count_launches(1);
   return cudaGetLastError();
@@ -452,10 +464,10 @@ cudaError_t launch_decode_down(const DecodeArgs& a, cudaStream_t s) {
   auto* hb = static_cast<const __nv_bfloat16*>(a.h);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_down);
   switch (mt_for(a.T)) {
-    case 8: decode_down_kernel<8><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
-    case 4: decode_down_kernel<4><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
-    case 2: decode_down_kernel<2><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
-    default: decode_down_kernel<1><<<grid, 128, 0, s>>>(hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    case 8: launch_pdl(decode_down_kernel<8>, grid, 128, 0, s, hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    case 4: launch_pdl(decode_down_kernel<4>, grid, 128, 0, s, hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    case 2: launch_pdl(decode_down_kernel<2>, grid, 128, 0, s, hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
+    default: launch_pdl(decode_down_kernel<1>, grid, 128, 0, s, hb, a.H, a.I, w, a.offsets, a.touched, a.sorted_f, a.topk_w, a.Y); break;
   }
   count_launches(1);
   return cudaGetLastError();
@@ -469,10 +481,10 @@ cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk
   auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   switch (mt_for(a.T)) {
-    case 8: decode_fused_gate_up_kernel<8><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    case 4: decode_fused_gate_up_kernel<4><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    case 2: decode_fused_gate_up_kernel<2><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    default: decode_fused_gate_up_kernel<1><<<grid, 128, 0, s>>>(hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 8: launch_pdl(decode_fused_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 4: launch_pdl(decode_fused_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 2: launch_pdl(decode_fused_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    default: launch_pdl(decode_fused_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
   }
   count_launches(1);
   return cudaGetLastError();
@@ -488,10 +500,10 @@ cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_id
   auto* w = static_cast<const __nv_bfloat16*>(a.w_down);
   auto* o = static_cast<__nv_bfloat16*>(a.out);
   switch (mt_for(a.T)) {
-    case 8: decode_fused_down_kernel<8><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
-    case 4: decode_fused_down_kernel<4><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
-    case 2: decode_fused_down_kernel<2><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
-    default: decode_fused_down_kernel<1><<<grid, 128, 0, s>>>(hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    case 8: launch_pdl(decode_fused_down_kernel<8>, grid, 128, 0, s, hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    case 4: launch_pdl(decode_fused_down_kernel<4>, grid, 128, 0, s, hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    case 2: launch_pdl(decode_fused_down_kernel<2>, grid, 128, 0, s, hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
+    default: launch_pdl(decode_fused_down_kernel<1>, grid, 128, 0, s, hb, a.T, a.H, a.I, a.k, a.E, n, w, topk_idx, a.topk_w, o, err); break;
   }
   count_launches(1);
   return cudaGetLastError();
@@ -502,7 +514,7 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   const long want = (total + 255) / 256;
   const long slots = static_cast<long>(a.num_sms) * 16;
   const int grid = static_cast<int>(want < slots ? want : slots);
-  decode_combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(a.Y), a.row_of, a.T,
+  launch_pdl(decode_combine_kernel, grid, 256, 0, s, reinterpret_cast<const float4*>(a.Y), a.row_of, a.T,
                                              a.H, a.k, static_cast<uint2*>(a.out));
   count_launches(1);
   return cudaGetLastError();

@@ -110,10 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
-  for (int i = threadIdx.x; i <= E; i += kThreads) {
-    s_off[i] = p.offsets[i];
-    s_pref[i] = p.tile_pref[i];
-  }
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -132,6 +129,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_b);
   }
   if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  // everything above touched only this CTA's shared memory, TMEM and the
+  // kernel parameters; the previous kernel's outputs are read from here on
+  pdl_wait();
+  for (int i = threadIdx.x; i <= E; i += kThreads) {
+    s_off[i] = p.offsets[i];
+    s_pref[i] = p.tile_pref[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -338,7 +342,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.out32 = a.out32;
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
-  kern<<<a.num_sms, kThreads, L::SMEM, s>>>(*a.tm_a, *a.tm_b, p);
+  launch_pdl(kern, a.num_sms, kThreads, L::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -415,8 +415,8 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
       if ((e = launch_gather_fp8(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), ue,
                                  xq, xs, s)) != cudaSuccess)
         return cuda_fail(e, "gather_fp8");
-      if ((e = cudaMemsetAsync(out32, 0, static_cast<size_t>(T) * H * 4, s)) != cudaSuccess)
-        return cuda_fail(e, "memset");
+      if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
+        return cuda_fail(e, "zero out32");
     }
     GroupedGemmFp8Args g{};
     g.offsets = d.offsets;
@@ -495,8 +495,8 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     if ((e = launch_gather_bf16(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), xa,
                                 s)) != cudaSuccess)
       return cuda_fail(e, "gather");
-    if ((e = cudaMemsetAsync(out32, 0, static_cast<size_t>(T) * H * 4, s)) != cudaSuccess)
-      return cuda_fail(e, "memset");
+    if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
+      return cuda_fail(e, "zero out32");
   }
   GroupedGemmArgs g{};
   g.offsets = d.offsets;

@@ -6,9 +6,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe_experts.h"
 
 namespace moe {
+
+// Every kernel of the library is launched with programmatic stream
+// serialisation allowed (programmatic dependent launch): its CTAs may be
+// scheduled while the previous kernel on the stream is still finishing, and
+// each kernel executes griddepcontrol.wait before its first global-memory
+// access, which blocks until that previous grid has completed and its
+// writes are visible.  What overlaps is launch latency and the shared-memory
+// and TMEM set-up, never a data dependence.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Error word bits written by kernels into the head of the workspace.
 enum : int {
@@ -70,6 +95,9 @@ cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sort
 cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
                               const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
                               cudaStream_t s);
+// out[0:n] = 0 (n a multiple of 4), as a kernel so it takes part in the
+// programmatic launch chain.
+cudaError_t launch_zero_f32(float* out, long n, cudaStream_t s);
 cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s);
 cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, bool ue8m0,
                                    uint8_t* q, void* scale, cudaStream_t s);

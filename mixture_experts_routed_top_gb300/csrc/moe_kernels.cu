@@ -20,6 +20,8 @@ template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
                                                     int k, int32_t* __restrict__ topk_idx,
                                                     float* __restrict__ topk_w) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long t = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -78,12 +80,12 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
   if (T == 0) return cudaSuccess;
   const int npl = ceil_div(E, 32);
   dim3 block(256), grid(ceil_div(static_cast<long>(T) * 32, 256));
-  if (npl <= 1) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
-  else if (npl <= 2) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
-  else if (npl <= 4) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
-  else if (npl <= 8) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
-  else if (npl <= 16) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
-  else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, idx, w);
+  if (npl <= 1) launch_pdl(route_kernel<1>, grid, block, 0, s, logits, T, E, k, idx, w);
+  else if (npl <= 2) launch_pdl(route_kernel<2>, grid, block, 0, s, logits, T, E, k, idx, w);
+  else if (npl <= 4) launch_pdl(route_kernel<4>, grid, block, 0, s, logits, T, E, k, idx, w);
+  else if (npl <= 8) launch_pdl(route_kernel<8>, grid, block, 0, s, logits, T, E, k, idx, w);
+  else if (npl <= 16) launch_pdl(route_kernel<16>, grid, block, 0, s, logits, T, E, k, idx, w);
+  else launch_pdl(route_kernel<32>, grid, block, 0, s, logits, T, E, k, idx, w);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -98,6 +100,8 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
 __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ idx,
                                                              long n, long chunk, int E,
                                                              int* blk_counts, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -123,6 +127,8 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks, int* blk_counts,
                                                              int* counts, int* offsets,
                                                              int* tile_pref, int* touched) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int s_warp[33];
   __shared__ int s_tot[kMaxE];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks,
 __global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __restrict__ idx, long n,
                                                             long chunk, int E, const int* blk_base,
                                                             int* sorted_f, int* row_of) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int cursor[kMaxE];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) cursor[e] = blk_base[static_cast<long>(blockIdx.x) * E + e];
@@ -203,12 +211,12 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
   const long chunk = dispatch_chunk(n);
   const int nchunks = n ? ceil_div(n, chunk) : 0;
   if (nchunks) {
-    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, n, chunk, E, d.blk_counts, d.err);
+    launch_pdl(dispatch_count_kernel, nchunks, 256, 0, s, topk_idx, n, chunk, E, d.blk_counts, d.err);
   }
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(E, nchunks, d.blk_counts, d.counts, d.offsets,
+  launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, E, nchunks, d.blk_counts, d.counts, d.offsets,
                                           d.tile_pref, d.touched);
   if (nchunks) {
-    dispatch_place_kernel<<<nchunks, 32, 0, s>>>(topk_idx, n, chunk, E, d.blk_counts,
+    launch_pdl(dispatch_place_kernel, nchunks, 32, 0, s, topk_idx, n, chunk, E, d.blk_counts,
                                                  d.sorted_f, d.row_of);
   }
   count_launches(nchunks ? 3 : 1);
@@ -222,6 +230,8 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restric
                                                           int k, const int* __restrict__ sorted_f,
                                                           const int* __restrict__ nvalid, int rows,
                                                           uint4* __restrict__ xperm) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (r >= rows || r >= *nvalid) return;
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restric
 cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,
                                const int* nvalid, int rows, void* x_perm, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  gather_bf16_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4*>(hidden), H / 8, k,
+  launch_pdl(gather_bf16_kernel, ceil_div(rows, 8), 256, 0, s, static_cast<const uint4*>(hidden), H / 8, k,
                                                        sorted_f, nvalid, rows,
                                                        static_cast<uint4*>(x_perm));
   count_launches(1);
@@ -283,6 +293,8 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict
                                                          const int* __restrict__ nvalid, int rows,
                                                          bool ue8m0, uint2* __restrict__ xq,
                                                          void* __restrict__ xs) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
   const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -336,7 +348,7 @@ cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorte
                               const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
                               cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  gather_fp8_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4*>(hidden), H, k,
+  launch_pdl(gather_fp8_kernel, ceil_div(rows, 8), 256, 0, s, static_cast<const uint4*>(hidden), H, k,
                                                       sorted_f, nvalid, rows, ue8m0,
                                                       reinterpret_cast<uint2*>(xq), xs);
   count_launches(1);
@@ -344,8 +356,32 @@ cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorte
 }
 
 // ============================================================== finish
+// out[0:4*n4] = 0.
+__global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ out, long n4) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+    out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+cudaError_t launch_zero_f32(float* out, long n, cudaStream_t s) {
+  const long n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long want = (n4 + 255) / 256;
+  const long cap = static_cast<long>(sms > 0 ? sms : 148) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  count_launches(1);
+  return launch_pdl(zero_f32_kernel, grid, 256, 0, s, reinterpret_cast<float4*>(out), n4);
+}
+
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src,
                                                       uint2* __restrict__ dst, long n4) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
     const float4 v = __ldg(src + i);
@@ -358,7 +394,7 @@ cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s) 
   if (n4 == 0) return cudaSuccess;
   const long want = (n4 + 255) / 256;
   const int grid = static_cast<int>(want < 152L * 16 ? want : 152L * 16);
-  to_bf16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+  launch_pdl(to_bf16_kernel, grid, 256, 0, s, reinterpret_cast<const float4*>(src),
                                       reinterpret_cast<uint2*>(dst), n4);
   count_launches(1);
   return cudaGetLastError();
@@ -371,6 +407,8 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(const uint4* __res
                                                               int cols, bool ue8m0,
                                                               uint2* __restrict__ q,
                                                               void* __restrict__ scale) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float s_max[8];
   const int nbc = cols / 128, nbr = rows / 128;
   const long blk = blockIdx.x;  // over nmat * nbr * nbc
@@ -416,7 +454,7 @@ cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, 
                                    uint8_t* q, void* scale, cudaStream_t s) {
   const long nblk = static_cast<long>(nmat) * (rows / 128) * (cols / 128);
   if (nblk == 0) return cudaSuccess;
-  quantize_blocks_kernel<<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+  launch_pdl(quantize_blocks_kernel, static_cast<unsigned>(nblk), 256, 0, s, 
       static_cast<const uint4*>(w), rows, cols, ue8m0, reinterpret_cast<uint2*>(q), scale);
   count_launches(1);
   return cudaGetLastError();
@@ -426,6 +464,8 @@ cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, 
 // Waits on an mbarrier that nothing completes; the bounded wait must give up
 // after limit_us, set the error word and return.
 __global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort;
   if (threadIdx.x != 0) return;
@@ -436,7 +476,7 @@ __global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
 }
 
 cudaError_t launch_selftest_wait(int* err, int limit_us, cudaStream_t s) {
-  selftest_wait_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+  launch_pdl(selftest_wait_kernel, 1, 32, 0, s, err, static_cast<uint64_t>(limit_us) * 1000ull);
   count_launches(1);
   return cudaGetLastError();
 }
