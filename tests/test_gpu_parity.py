@@ -165,6 +165,7 @@ def test_forward_bf16_one_expert_takes_all(moe, path):
     MoEShape(T=16, H=256, I=128, E=4, k=1),        # several tokens per expert
     MoEShape(T=16, H=128, I=256, E=1, k=1),        # 16 tokens on one expert: 2 token chunks
     MoEShape(T=4, H=2048, I=1408, E=60, k=4),      # Qwen width at the default threshold
+    MoEShape(T=8, H=256, I=2048, E=8, k=4),        # the widest h rows (2048) at 8 tokens per expert
 ])
 def test_forward_bf16_fused_decode(moe, shape, path):
     """Few routed rows: the two fused decode kernels run (two launches, no
