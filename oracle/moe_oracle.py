@@ -12,8 +12,8 @@ The "eager" row of the backends table describes the plain form this oracle
 follows: loop over the selected experts and apply the projections to their
 tokens.  The gated MLP is "up projection, SwiGLU, down projection" (the
 deepgemm_megamoe row of the backends table and the "Fused Mega MoE on
-Blackwell" section); the SonicMoE section maps the gate activation silu to
-SwiGLU.  FP8 experts carry float32 or UE8M0 block scales (paragraph after the
+Blackwell" section); the SonicMoE section maps the gate activations silu,
+gelu and relu to SwiGLU, GeGLU and ReGLU.  FP8 experts carry float32 or UE8M0 block scales (paragraph after the
 backends table) and activations take dynamic per-row scales ("FP8 and FP4
 quantized experts" section).
 
@@ -27,6 +27,9 @@ project's design notes:
   * fused gate/up weight W_gate_up[e] is [2I, H], rows 0..I-1 gate and rows
     I..2I-1 up; W_down[e] is [H, I] (the [out, in] convention);
   * SwiGLU: h = silu(g) * u, silu(x) = x / (1 + exp(-x)), no bias, no clamp;
+    GeGLU: h = gelu(g) * u with the exact GELU x * Phi(x) = x/2 (1 + erf(x/sqrt 2))
+    (the page says only "gelu"; the tanh approximation is a different name);
+    ReGLU: h = max(g, 0) * u;
   * combine: out[t] = sum_j w[t,j] * y[t,j], summed in the oracle's float
     type and rounded once to bf16 (round to nearest even);
   * dispatch: expert-contiguous rows, stable in the flat index f = t*k + j;
@@ -46,7 +49,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "route", "route_weights_full_softmax", "dispatch", "silu",
+    "route", "route_weights_full_softmax", "dispatch", "silu", "gelu", "relu",
+    "ACTIVATIONS",
     "expert_mlp", "forward", "forward_brute", "round_to_bf16",
     "bf16_bits_to_f32", "e4m3_encode", "e4m3_decode", "ue8m0_from_quotient",
     "quantize_blocks", "dequantize_blocks", "forward_fp8",
@@ -169,10 +173,34 @@ def silu(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def _erf(x: np.ndarray) -> np.ndarray:
+    try:
+        from scipy.special import erf
+        return erf(x)
+    except ImportError:                      # plain per-element fallback
+        import math
+        return np.vectorize(math.erf, otypes=[np.float64])(x)
+
+
+def gelu(x: np.ndarray) -> np.ndarray:
+    """Exact GELU: x * Phi(x) = x/2 * (1 + erf(x / sqrt(2)))."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + _erf(x / np.sqrt(2.0)))
+
+
+def relu(x: np.ndarray) -> np.ndarray:
+    """max(x, 0)."""
+    return np.maximum(np.asarray(x), 0.0)
+
+
+# gate activation of the gated MLP, by name: SwiGLU, GeGLU, ReGLU
+ACTIVATIONS = {"silu": silu, "gelu": gelu, "relu": relu}
+
+
 def expert_mlp(x: np.ndarray, w_gate_up_e: np.ndarray, w_down_e: np.ndarray,
-               dtype=np.float64) -> np.ndarray:
+               dtype=np.float64, act: str = "silu") -> np.ndarray:
     """One expert's gated MLP on rows x [M, H]: g = x Wg^T, u = x Wu^T,
-    h = silu(g) * u, y = h Wd^T.  Returns y [M, H] in ``dtype``."""
+    h = act(g) * u, y = h Wd^T.  Returns y [M, H] in ``dtype``."""
     I = w_gate_up_e.shape[0] // 2
     x = np.asarray(x, dtype=dtype)
     wg = np.asarray(w_gate_up_e[:I], dtype=dtype)
@@ -180,19 +208,20 @@ def expert_mlp(x: np.ndarray, w_gate_up_e: np.ndarray, w_down_e: np.ndarray,
     wd = np.asarray(w_down_e, dtype=dtype)
     g = x @ wg.T
     u = x @ wu.T
-    h = silu(g) * u
+    h = ACTIVATIONS[act](g) * u
     return h @ wd.T
 
 
 def forward(hidden: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
             w_gate_up: np.ndarray, w_down: np.ndarray, dtype=np.float64,
-            round_h_bf16: bool = False) -> np.ndarray:
+            round_h_bf16: bool = False, act: str = "silu") -> np.ndarray:
     """Eager loop over experts (the "eager" backend's plain form).
 
     hidden [T,H], w_gate_up [E,2I,H], w_down [E,H,I] as float arrays holding
     the bf16 values; topk_idx [T,k]; topk_w [T,k].  Returns the un-rounded
     output [T,H] in ``dtype``; apply round_to_bf16 for the stored output.
-    ``round_h_bf16`` rounds the intermediate h to bf16 (diagnostic only)."""
+    ``round_h_bf16`` rounds the intermediate h to bf16 (diagnostic only);
+    ``act`` names the gate activation (silu, gelu or relu)."""
     T, H = hidden.shape
     E = w_gate_up.shape[0]
     k = topk_idx.shape[1]
@@ -211,7 +240,7 @@ def forward(hidden: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
         wu = np.asarray(w_gate_up[e, I:], dtype=dtype)
         g = x @ wg.T
         u = x @ wu.T
-        h = silu(g) * u
+        h = ACTIVATIONS[act](g) * u
         if round_h_bf16:
             h = round_to_bf16(h).astype(dtype)
         y = h @ np.asarray(w_down[e], dtype=dtype).T
@@ -219,7 +248,7 @@ def forward(hidden: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
     return out
 
 
-def forward_brute(hidden, topk_idx, topk_w, w_gate_up, w_down) -> np.ndarray:
+def forward_brute(hidden, topk_idx, topk_w, w_gate_up, w_down, act: str = "silu") -> np.ndarray:
     """Float64 loop over (token, slot) with explicit dot products, no
     dispatch and no batching; for tiny inputs only."""
     T, H = hidden.shape
@@ -234,7 +263,13 @@ def forward_brute(hidden, topk_idx, topk_w, w_gate_up, w_down) -> np.ndarray:
             for i in range(I):
                 g = float(np.dot(x, np.asarray(w_gate_up[e, i], np.float64)))
                 u = float(np.dot(x, np.asarray(w_gate_up[e, I + i], np.float64)))
-                s = g / (1.0 + np.exp(-g)) if g >= 0 else g * np.exp(g) / (1.0 + np.exp(g))
+                if act == "silu":
+                    s = g / (1.0 + np.exp(-g)) if g >= 0 else g * np.exp(g) / (1.0 + np.exp(g))
+                elif act == "gelu":
+                    import math
+                    s = 0.5 * g * (1.0 + math.erf(g / math.sqrt(2.0)))
+                else:
+                    s = g if g > 0 else 0.0
                 h[i] = s * u
             for c in range(H):
                 out[t, c] += float(topk_w[t, j]) * float(
@@ -361,7 +396,7 @@ def scale_values(stored: np.ndarray, fmt: str) -> np.ndarray:
 
 def forward_fp8(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down,
                 ws_down, fmt: str, quantize_act: bool = True,
-                quantize_h: bool = True) -> np.ndarray:
+                quantize_h: bool = True, act: str = "silu") -> np.ndarray:
     """FP8 block-scaled forward, mirrored: the same dequantised weights and
     the same dynamic 1x128 activation quantisation as the device path, math
     in float64 otherwise.  wq_* are e4m3 codes, ws_* stored scales (fp32 or
@@ -388,7 +423,7 @@ def forward_fp8(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down,
         x = np.asarray(x, dtype=np.float64)
         g = x @ wgu[e, :I].T
         u = x @ wgu[e, I:].T
-        h = silu(g) * u
+        h = ACTIVATIONS[act](g) * u
         if quantize_h:
             hq, _, hs = quantize_blocks(h.astype(np.float32), 1, 128, fmt)
             h = dequantize_blocks(hq, hs, 1, 128)

@@ -136,30 +136,62 @@ def test_dispatch_empty_and_out_of_range():
 # forward
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("act", ["silu", "gelu", "relu"])
 @pytest.mark.parametrize("shape", [MoEShape(T=7, H=32, I=16, E=4, k=2),
                                    MoEShape(T=12, H=64, I=64, E=8, k=3),
                                    MoEShape(T=5, H=16, I=48, E=3, k=3)])
-def test_forward_vs_brute_force(shape):
+def test_forward_vs_brute_force(shape, act):
     logits, hidden, wgu, wd = _np_inputs(shape)
     idx, w = O.route(logits, shape.k)
-    out = O.forward(hidden, idx, w, wgu, wd)
-    ref = O.forward_brute(hidden, idx, w, wgu, wd)
+    out = O.forward(hidden, idx, w, wgu, wd, act=act)
+    ref = O.forward_brute(hidden, idx, w, wgu, wd, act=act)
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(out - ref)) / rms < 1e-10
 
 
-def test_forward_single_expert_is_dense_swiglu():
+# torch's CPU activations as the library routine the gated MLP reduces to
+_TORCH_ACT = {"silu": torch.nn.functional.silu,
+              "gelu": lambda x: torch.nn.functional.gelu(x, approximate="none"),
+              "relu": torch.relu}
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu", "relu"])
+def test_forward_single_expert_is_dense_glu(act):
+    """E = 1, k = 1: the forward is one dense gated MLP (SwiGLU, GeGLU or
+    ReGLU), computed here with torch's linear and activation on the CPU."""
     shape = MoEShape(T=33, H=64, I=96, E=1, k=1)
     logits, hidden, wgu, wd = _np_inputs(shape)
     idx, w = O.route(logits, 1)
     assert np.all(idx == 0) and np.allclose(w, 1.0)
-    out = O.forward(hidden, idx, w, wgu, wd, dtype=np.float32)
+    out = O.forward(hidden, idx, w, wgu, wd, dtype=np.float32, act=act)
     x = torch.from_numpy(hidden)
     g = torch.nn.functional.linear(x, torch.from_numpy(wgu[0, :96]))
     u = torch.nn.functional.linear(x, torch.from_numpy(wgu[0, 96:]))
-    ref = torch.nn.functional.linear(torch.nn.functional.silu(g) * u,
+    ref = torch.nn.functional.linear(_TORCH_ACT[act](g) * u,
                                      torch.from_numpy(wd[0])).numpy()
     assert O.rel_max_err(out, ref) < 1e-5
+
+
+def test_gelu_closed_forms():
+    """Exact GELU = x * Phi(x): Phi(1) = 0.8413447460685429 (normal table),
+    gelu(x) - gelu(-x) = x (Phi(x) + Phi(-x) = 1), gelu(0) = 0, gelu(x) -> x
+    and -> 0 in the tails; and torch's exact gelu in float64."""
+    assert O.gelu(np.array([1.0]))[0] == pytest.approx(0.8413447460685429, rel=1e-15)
+    assert O.gelu(np.array([-1.0]))[0] == pytest.approx(-0.15865525393145707, rel=1e-14)
+    x = np.linspace(-9.0, 9.0, 1001)
+    np.testing.assert_allclose(O.gelu(x) - O.gelu(-x), x, rtol=0, atol=1e-14)
+    assert O.gelu(np.array([0.0]))[0] == 0.0
+    assert abs(O.gelu(np.array([12.0]))[0] - 12.0) < 1e-15
+    assert abs(O.gelu(np.array([-12.0]))[0]) < 1e-15
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="none").numpy()
+    np.testing.assert_allclose(O.gelu(x), ref, rtol=1e-14, atol=1e-15)
+
+
+def test_relu_and_silu_against_torch():
+    x = np.linspace(-30.0, 30.0, 2001)
+    np.testing.assert_array_equal(O.relu(x), torch.relu(torch.from_numpy(x)).numpy())
+    np.testing.assert_allclose(O.silu(x), torch.nn.functional.silu(torch.from_numpy(x)).numpy(),
+                               rtol=1e-14, atol=1e-300)
 
 
 def test_forward_k_equals_E_uniform_is_mean_of_experts():
@@ -301,17 +333,18 @@ def _fp8_weights(wgu, wd, fmt):
     return qgu, sgu, qd, sd
 
 
-@pytest.mark.parametrize("fmt", ["f32", "ue8m0"])
-def test_fp8_forward_without_act_quant_is_bf16_oracle_on_dequantised_weights(fmt):
+@pytest.mark.parametrize("fmt,act", [("f32", "silu"), ("ue8m0", "silu"), ("f32", "gelu"),
+                                     ("ue8m0", "relu")])
+def test_fp8_forward_without_act_quant_is_bf16_oracle_on_dequantised_weights(fmt, act):
     shape = MoEShape(T=24, H=256, I=128, E=4, k=2)
     logits, hidden, wgu, wd = _np_inputs(shape)
     idx, w = O.route(logits, 2)
     qgu, sgu, qd, sd = _fp8_weights(wgu, wd, fmt)
     out8 = O.forward_fp8(hidden, idx, w, qgu, sgu, qd, sd, fmt,
-                         quantize_act=False, quantize_h=False)
+                         quantize_act=False, quantize_h=False, act=act)
     wgu_d = O.dequantize_blocks(qgu, O.scale_values(sgu, fmt), 128, 128)
     wd_d = O.dequantize_blocks(qd, O.scale_values(sd, fmt), 128, 128)
-    ref = O.forward(hidden, idx, w, wgu_d, wd_d)
+    ref = O.forward(hidden, idx, w, wgu_d, wd_d, act=act)
     np.testing.assert_allclose(out8, ref, rtol=1e-12, atol=1e-14)
 
 
