@@ -282,10 +282,11 @@ class OracleSample:
         t0 = time.perf_counter()
         idx, wt = O.route(self.logits, self.k)
         lidx = self.remap[idx].astype("int32")
+        act = self.w.get("act", "silu")
         if self.w["wfmt"] == "fp8":
-            O.forward_fp8(self.hid, lidx, wt, *self.parts, self.w["sfmt"])
+            O.forward_fp8(self.hid, lidx, wt, *self.parts, self.w["sfmt"], act=act)
         else:
-            O.forward(self.hid, lidx, wt, *self.parts)
+            O.forward(self.hid, lidx, wt, *self.parts, act=act)
         return time.perf_counter() - t0
 
 
@@ -315,6 +316,7 @@ def run_ours(args, rank, world, local_rank):
     moe.lib(build_if_missing=True)
     moe.set_swap_rows({"auto": -1, "rows": 0, "swap": 1 << 20}[args.bf16_gemm])
     w = build_workload(args.workload, dev)
+    w["act"] = args.activation
     s = w["shape"]
     W = weights_of(w)
     ws = moe.Workspace(dev)
@@ -323,7 +325,8 @@ def run_ours(args, rank, world, local_rank):
 
     def step(logits, hidden, dst=None):
         idx, wt = moe.route(logits, s.k)
-        moe.experts_forward(hidden, idx, wt, out=out if dst is None else dst, workspace=ws, **W)
+        moe.experts_forward(hidden, idx, wt, out=out if dst is None else dst, workspace=ws,
+                            activation=args.activation, **W)
         return idx
 
     # routing statistics of the workload (outside any timed region)
@@ -539,7 +542,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("flushed before every timed step (512 MB write)" if flush else
                           f"inputs larger than L2 ({working_set / 1e9:.2f} GB touched per step)"),
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
-                   "bf16_gemm": args.bf16_gemm,
+                   "bf16_gemm": args.bf16_gemm, "activation": args.activation,
                    "timed_steps": "CUDA graph replays of one captured step" if args.graph
                                   else "steps launched from Python",
                    "stage_timing": ("per-stage CUDA events in a second capture of the same "
@@ -579,6 +582,8 @@ def main():
                     help="launch every timed step from Python instead of replaying a CUDA graph")
     ap.add_argument("--bf16-gemm", default="auto", choices=["auto", "rows", "swap"],
                     help="orientation of the bf16 grouped GEMMs (library default: auto)")
+    ap.add_argument("--activation", default="silu", choices=["silu", "gelu", "relu"],
+                    help="gate activation: SwiGLU (default), GeGLU or ReGLU experts")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -621,6 +626,7 @@ def run_reference(args):
                           "unavailable": "the fp8 workload builds its weights with the GPU quantiser"}))
         return 0
     w = build_workload(args.workload, dev)
+    w["act"] = args.activation
     s = w["shape"]
     smp, _ = calibrated_oracle_sample(w, budget_s=2.0)
     for _ in range(args.warmup):
@@ -632,8 +638,10 @@ def run_reference(args):
             "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": args.workload, "T": s.T, "H": s.H, "I": s.I, "E": s.E,
-                       "k": s.k},
+            "config": {"workload": args.workload,
+                       "description": DESCRIPTIONS[WORKLOADS[args.workload][0]],
+                       "T": s.T, "H": s.H, "I": s.I, "E": s.E, "k": s.k,
+                       "scale_fmt": w["sfmt"], "activation": args.activation},
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
                              "cores": blas_threads(), "kind": "oracle",
                              "sample": f"each step: first {smp.n} tokens of the workload "

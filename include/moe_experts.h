@@ -135,6 +135,31 @@ moe_status moe_experts_forward(const void* hidden, int T, int H,
                                void* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Gate activation of the gated expert MLP (SonicMoE section: silu, gelu and
+ * relu map to SwiGLU, GeGLU and ReGLU): h = act(gate x) * (up x).
+ *   MOE_ACT_SILU  silu(x) = x / (1 + e^-x)            (SwiGLU)
+ *   MOE_ACT_GELU  exact GELU x/2 (1 + erf(x / sqrt 2)) (GeGLU)
+ *   MOE_ACT_RELU  max(x, 0)                            (ReGLU)
+ */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_GELU = 1, MOE_ACT_RELU = 2 } moe_activation;
+
+/*
+ * moe_experts_forward_act - moe_experts_forward with the gate activation as
+ * an argument; moe_experts_forward is this call with MOE_ACT_SILU.  Every
+ * path (token-row and swap-AB grouped GEMMs, FP8, decode) applies it in the
+ * gate/up epilogue.  An activation outside moe_activation:
+ * MOE_ERR_INVALID_ARG.  Everything else as moe_experts_forward.
+ */
+moe_status moe_experts_forward_act(const void* hidden, int T, int H,
+                                   const int32_t* topk_idx, const float* topk_w,
+                                   int E, int k, int I,
+                                   const void* w_gate_up, const void* w_down,
+                                   moe_wdtype wdtype,
+                                   const void* scale_gate_up, const void* scale_down,
+                                   moe_scale_fmt sfmt, moe_activation act,
+                                   void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_quantize_fp8_blocks - quantise bf16 matrices into e4m3 codes with one
  * scale per 128x128 block (the FP8 expert format of the "FP8 and FP4
  * quantized experts" section).  Scale s = amax/448 (float32 division) for

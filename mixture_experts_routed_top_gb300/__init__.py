@@ -22,7 +22,7 @@ __all__ = [
     "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
     "selftest_wait_timeout", "launch_count",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
-    "SCALE_UE8M0",
+    "SCALE_UE8M0", "ACTIVATIONS",
 ]
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -51,6 +51,8 @@ _SIGS = {
     "moe_workspace_size": ([_I, _I, _I, _I, _I, _I], _SZ),
     "moe_experts_forward": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P,
                              _SZ, _P], _I),
+    "moe_experts_forward_act": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P,
+                                 _P, _SZ, _P], _I),
     "moe_quantize_fp8_blocks": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_workspace_status": ([_P, _P], _I),
     "moe_set_decode_rows": ([_I], None),
@@ -166,18 +168,23 @@ class Workspace:
 
 _DEFAULT_WS = {}
 
+# moe_activation values
+ACTIVATIONS = {"silu": 0, "gelu": 1, "relu": 2}
+
 
 def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                     w_gate_up: torch.Tensor, w_down: torch.Tensor,
                     scale_gate_up: Optional[torch.Tensor] = None,
                     scale_down: Optional[torch.Tensor] = None, scale_fmt=None,
                     out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
-                    stream=None) -> torch.Tensor:
+                    stream=None, activation: str = "silu") -> torch.Tensor:
     """Routed experts forward -> bf16 [T, H].
 
     hidden bf16 [T,H]; topk_idx int32 [T,k]; topk_w fp32 [T,k];
     w_gate_up [E,2I,H] and w_down [E,H,I], bf16 or e4m3 bytes (uint8 or
-    float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0')."""
+    float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0');
+    activation: the gate activation, 'silu' (SwiGLU), 'gelu' (GeGLU, exact
+    erf GELU) or 'relu' (ReGLU)."""
     _need_cuda(hidden, topk_idx, topk_w, w_gate_up, w_down, scale_gate_up, scale_down, out)
     T, H = hidden.shape
     k = topk_idx.shape[1]
@@ -201,10 +208,12 @@ def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.
         if workspace is None:
             workspace = _DEFAULT_WS.setdefault(key, Workspace(key))
     ws = workspace.get(nbytes)
-    _check(lib().moe_experts_forward(
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    _check(lib().moe_experts_forward_act(
         _ptr(hidden), T, H, _ptr(topk_idx), _ptr(topk_w), E, k, I, _ptr(w_gate_up),
-        _ptr(w_down), wdtype, _ptr(scale_gate_up), _ptr(scale_down), sf, _ptr(out), _ptr(ws),
-        ws.numel(), _stream(stream)))
+        _ptr(w_down), wdtype, _ptr(scale_gate_up), _ptr(scale_down), sf, ACTIVATIONS[activation],
+        _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(128) decode_gate_up_kernel(
     const __nv_bfloat16* __restrict__ hidden, int H, int I, int k,
     const __nv_bfloat16* __restrict__ wgu, const int* __restrict__ offsets,
     const int* __restrict__ touched, const int* __restrict__ sorted_f,
-    __nv_bfloat16* __restrict__ h_out) {
+    __nv_bfloat16* __restrict__ h_out, int act) {
   pdl_launch_dependents();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(128) decode_gate_up_kernel(
         const float g = warp_sum(ag[t]);
         const float u = warp_sum(au[t]);
         if (lane == 0 && t0 + t < m)
-          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(silu_f(g) * u);
+          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(gate_act(g, act) * u);
       }
     }
   }
@@ -336,7 +336,7 @@ template <int MT>
 __global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
     const __nv_bfloat16* __restrict__ hidden, int H, int I, int k, int E, int n,
     const __nv_bfloat16* __restrict__ wgu, const int32_t* __restrict__ topk_idx,
-    __nv_bfloat16* __restrict__ h_out, int* err) {
+    __nv_bfloat16* __restrict__ h_out, int* err, int act) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ SmallTable tab;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
         const float gs = warp_sum(ag[t]);
         const float us = warp_sum(au[t]);
         if (lane == 0 && t0 + t < m)
-          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(silu_f(gs) * us);
+          h_out[static_cast<long>(r0 + t0 + t) * I + f] = __float2bfloat16_rn(gate_act(gs, act) * us);
       }
     }
   }
@@ -450,10 +450,10 @@ cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s) {
   auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   switch (mt_for(a.T)) {
-    case 8: launch_pdl(decode_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    case 4: launch_pdl(decode_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    case 2: launch_pdl(decode_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
-    default: launch_pdl(decode_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb); break;
+    case 8: launch_pdl(decode_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb, a.act); break;
+    case 4: launch_pdl(decode_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb, a.act); break;
+    case 2: launch_pdl(decode_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb, a.act); break;
+    default: launch_pdl(decode_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, w, a.offsets, a.touched, a.sorted_f, hb, a.act); break;
   }
   count_launches(1);
   return cudaGetLastError();
@@ -481,10 +481,10 @@ cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk
   auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   switch (mt_for(a.T)) {
-    case 8: launch_pdl(decode_fused_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    case 4: launch_pdl(decode_fused_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    case 2: launch_pdl(decode_fused_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
-    default: launch_pdl(decode_fused_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err); break;
+    case 8: launch_pdl(decode_fused_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    case 4: launch_pdl(decode_fused_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    case 2: launch_pdl(decode_fused_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    default: launch_pdl(decode_fused_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
   }
   count_launches(1);
   return cudaGetLastError();

@@ -75,6 +75,7 @@ struct Fp8Dev {
   float* out32;         // down: [T, H]
   const int* sorted_f;
   const float* topk_w;
+  int act;              // moe_activation of the gate/up epilogue
 };
 
 __device__ __forceinline__ void decode_tile8(int tile, int NT, int E, const int* s_pref, int& e,
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          acc0[i] = silu_f(acc0[i]) * acc1[i];
+          acc0[i] = gate_act(acc0[i], p.act) * acc1[i];
           amax = fmaxf(amax, fabsf(acc0[i]));
         }
         float* am = s_amax + (amax_phase ? kEpiGroups * 128 : 0);   // double-buffered by tile
@@ -478,6 +479,7 @@ cudaError_t launch_fp8_impl(const GroupedGemmFp8Args& a, cudaStream_t s) {
   p.out32 = a.out32;
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
+  p.act = a.act;
   launch_pdl(kern, a.num_sms, kThreads, L8::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

@@ -67,6 +67,7 @@ struct GemmDev {
   float* out32;
   const int* sorted_f;
   const float* topk_w;
+  int act;             // moe_activation of the gate/up epilogue
 };
 
 __device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* s_pref, int& e,
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            pk[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+            pk[i] = pack_bf16x2(gate_act(g0, p.act) * u0, gate_act(g1, p.act) * u1);
           }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
@@ -342,6 +343,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.out32 = a.out32;
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
+  p.act = a.act;
   launch_pdl(kern, a.num_sms, kThreads, L::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

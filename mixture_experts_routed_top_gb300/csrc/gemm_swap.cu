@@ -62,6 +62,7 @@ struct GemmDev {
   float* out32;
   const int* sorted_f;
   const float* topk_w;
+  int act;               // moe_activation of the gate/up epilogue
 };
 
 struct Tile {
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             if (i < cnt) {
               const float g = __uint_as_float(d0[i]), u = __uint_as_float(d1[i]);
-              dst[static_cast<long>(i) * p.I] = __float2bfloat16_rn(silu_f(g) * u);
+              dst[static_cast<long>(i) * p.I] = __float2bfloat16_rn(gate_act(g, p.act) * u);
             }
           }
         } else {
@@ -336,6 +337,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.out32 = a.out32;
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
+  p.act = a.act;
   launch_pdl(kern, a.num_sms, kThreads, SMEM_BYTES, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

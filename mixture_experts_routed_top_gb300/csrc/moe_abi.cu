@@ -280,7 +280,21 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
                                const void* w_down, moe_wdtype wdtype, const void* scale_gate_up,
                                const void* scale_down, moe_scale_fmt sfmt, void* out, void* ws,
                                size_t ws_bytes, void* stream) {
+  return moe_experts_forward_act(hidden, T, H, topk_idx, topk_w, E, k, I, w_gate_up, w_down,
+                                 wdtype, scale_gate_up, scale_down, sfmt, MOE_ACT_SILU, out, ws,
+                                 ws_bytes, stream);
+}
+
+moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32_t* topk_idx,
+                                   const float* topk_w, int E, int k, int I,
+                                   const void* w_gate_up, const void* w_down, moe_wdtype wdtype,
+                                   const void* scale_gate_up, const void* scale_down,
+                                   moe_scale_fmt sfmt, moe_activation act, void* out, void* ws,
+                                   size_t ws_bytes, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act != MOE_ACT_SILU && act != MOE_ACT_GELU && act != MOE_ACT_RELU)
+    return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: unknown activation %d",
+                static_cast<int>(act));
   if (T < 0 || H < 1 || I < 1) return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: bad sizes");
   if (E < 1 || E > kMaxE)
     return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: E must be in [1, %d]", kMaxE);
@@ -356,6 +370,7 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     a.E = E;
     a.k = k;
     a.num_sms = sms;
+    a.act = static_cast<int>(act);
     if (decode_fused_fits(a)) {
       // routing table rebuilt inside both kernels; the down kernel combines
       {
@@ -420,6 +435,7 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
     }
     GroupedGemmFp8Args g{};
     g.offsets = d.offsets;
+    g.act = static_cast<int>(act);
     g.tile_pref = d.tile_pref;
     g.E = E;
     g.I = I;
@@ -500,6 +516,7 @@ moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* 
   }
   GroupedGemmArgs g{};
   g.offsets = d.offsets;
+  g.act = static_cast<int>(act);
   g.tile_pref = d.tile_pref;
   g.E = E;
   g.I = I;

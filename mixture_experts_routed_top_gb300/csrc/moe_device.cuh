@@ -227,8 +227,22 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 // ---------------------------------------------------------------- misc
+// silu(g) = g / (1 + e^-g).  The fast division (2 ulp of fp32 for divisors
+// below 2^126) replaces the IEEE one: the result is rounded to bf16 or
+// e4m3 next, and the division was the costliest step of the gate/up
+// epilogue.  -g is clamped at 80 so the divisor stays in that range; below
+// g = -80 the result is under 2^-100 * |g| either way.
 __device__ __forceinline__ float silu_f(float g) {
-  return g / (1.0f + __expf(-g));
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f)));
+}
+
+// Gate activation of the gated MLP, `act` a moe_activation value (uniform
+// across the kernel, so the branch never diverges): silu, exact GELU
+// x/2 (1 + erf(x / sqrt 2)), or max(x, 0).
+__device__ __forceinline__ float gate_act(float g, int act) {
+  if (act == MOE_ACT_SILU) return silu_f(g);
+  if (act == MOE_ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f));
+  return fmaxf(g, 0.0f);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

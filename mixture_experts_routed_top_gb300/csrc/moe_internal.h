@@ -123,6 +123,7 @@ struct GroupedGemmArgs {
   const int* sorted_f;
   const float* topk_w;
   int num_sms;
+  int act;                   // moe_activation of the gate/up epilogue
 };
 cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
@@ -148,6 +149,7 @@ struct GroupedGemmFp8Args {
   const int* sorted_f;
   const float* topk_w;
   int num_sms;
+  int act;                   // moe_activation of the gate/up epilogue
 };
 cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
 cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
@@ -166,6 +168,7 @@ struct DecodeArgs {
   float* Y;                  // fp32 [T*k, H], weighted rows
   void* out;                 // bf16 [T, H]
   int T, H, I, E, k, num_sms;
+  int act;                   // moe_activation of the gate/up GEMV
 };
 constexpr int kDecodeRowsDefault = 16;    // T*k at or below: decode path (measured crossover)
 constexpr int kDecodeRowsMax = 2048;      // the decode path's workspace is sized up to this

@@ -66,6 +66,12 @@ def test_argument_errors_without_device(L):
     # workspace too small (checked before any launch); fake aligned pointers
     p = ctypes.c_void_p(1 << 20)
     assert f(p, 4, 128, p, p, 8, 2, 128, p, p, 0, nul, nul, 0, p, p, 16, nul) == 5
+    fa = L.moe_experts_forward_act
+    # unknown gate activation (checked first); the three named ones pass that check
+    assert fa(p, 4, 128, p, p, 8, 2, 128, p, p, 0, nul, nul, 0, 3, p, p, 16, nul) == 1
+    assert b"activation" in L.moe_last_error()
+    for act in (0, 1, 2):
+        assert fa(p, 4, 128, p, p, 8, 2, 128, p, p, 0, nul, nul, 0, act, p, p, 16, nul) == 5
     assert L.moe_quantize_fp8_blocks(nul, 1, 100, 128, 1, nul, nul, nul) == 2
     assert L.moe_quantize_fp8_blocks(nul, 1, 128, 128, 0, nul, nul, nul) == 1
 

@@ -45,7 +45,7 @@ def test_weight_quantiser_bit_exact(moe, fmt):
         assert np.array_equal(s.cpu().numpy(), rs)
 
 
-def _fp8_case(moe, shape, fmt, seed=0, logit_bias=None):
+def _fp8_case(moe, shape, fmt, seed=0, logit_bias=None, act="silu"):
     d = make_inputs(shape, seed=seed, device="cpu")
     logits = d["logits"] if logit_bias is None else d["logits"] + logit_bias
     idx, w = O.route(logits.numpy(), shape.k)
@@ -55,11 +55,13 @@ def _fp8_case(moe, shape, fmt, seed=0, logit_bias=None):
     out = moe.experts_forward(d["hidden"].cuda(), torch.from_numpy(idx).cuda(),
                               torch.from_numpy(w).cuda(), torch.from_numpy(qgu).cuda(),
                               torch.from_numpy(qd).cuda(), scale_gate_up=torch.from_numpy(sgu).cuda(),
-                              scale_down=torch.from_numpy(sd).cuda(), scale_fmt=fmt)
+                              scale_down=torch.from_numpy(sd).cuda(), scale_fmt=fmt,
+                              activation=act)
     moe.workspace_status(moe.default_workspace())
     hid = d["hidden"].float().numpy()
-    ref = O.forward_fp8(hid, idx, w, qgu, sgu, qd, sd, fmt)
-    plain = O.forward(hid, idx, w, d["w_gate_up"].float().numpy(), d["w_down"].float().numpy())
+    ref = O.forward_fp8(hid, idx, w, qgu, sgu, qd, sd, fmt, act=act)
+    plain = O.forward(hid, idx, w, d["w_gate_up"].float().numpy(), d["w_down"].float().numpy(),
+                      act=act)
     return out.float().cpu().numpy(), ref, plain
 
 
@@ -76,6 +78,15 @@ def test_forward_fp8_parity(moe, shape, fmt):
     assert np.all(np.isfinite(out))
     assert O.rel_max_err(out, ref) <= FP8_TOL
     # sanity, not a gate: the FP8 result stays near the unquantised forward
+    assert O.rel_max_err(out, plain) < 0.5
+
+
+@pytest.mark.parametrize("fmt,act", [("f32", "gelu"), ("ue8m0", "relu")])
+@pytest.mark.parametrize("shape", [MoEShape(T=300, H=512, I=384, E=6, k=3),
+                                   MoEShape(T=40, H=1024, I=512, E=64, k=6)])
+def test_forward_fp8_geglu_reglu(moe, shape, fmt, act):
+    out, ref, plain = _fp8_case(moe, shape, fmt, act=act)
+    assert O.rel_max_err(out, ref) <= FP8_TOL
     assert O.rel_max_err(out, plain) < 0.5
 
 
