@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int arow = s_off[e] + m * BM;
         const int brow = (EPI == EPI_SWIGLU) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
+          if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) {
         if ((issued >> s) & 1u) {
           volatile int no_abort = 0;
-          mbar_wait_bounded(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
+          mbar_wait_bounded<true>(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
                             ERR_TIMEOUT_PRODUCER, 20000000ull);
         }
       }
@@ -205,12 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aph ^ 1u, s_abort, p.err, ERR_TIMEOUT_MMA))
+        if (!mbar_wait_bounded<true>(smem_u32(&tempty[acc]), aph ^ 1u, s_abort, p.err, ERR_TIMEOUT_MMA))
           break;
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccCols;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
+          if (!mbar_wait_bounded<true>(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0) {
         umma_commit(smem_u32(fin));
         volatile int no_abort = 0;
-        mbar_wait_bounded(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
+        mbar_wait_bounded<true>(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
       }
     }
   } else {
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aph = (it >> 1) & 1;
       int ok = 1;
       if (lane == 0)
-        ok = mbar_wait_bounded(smem_u32(&tfull[acc]), aph, s_abort, p.err, ERR_TIMEOUT_EPILOGUE);
+        ok = mbar_wait_bounded<true>(smem_u32(&tfull[acc]), aph, s_abort, p.err, ERR_TIMEOUT_EPILOGUE);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();

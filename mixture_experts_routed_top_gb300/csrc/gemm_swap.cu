@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int wrow0, wrow1;
         weight_rows(t, wrow0, wrow1);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
+          if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) {  // drain: every issued load has landed
         if ((issued >> s) & 1u) {
           volatile int no_abort = 0;
-          mbar_wait_bounded(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
+          mbar_wait_bounded<true>(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
                             ERR_TIMEOUT_PRODUCER, 20000000ull);
         }
       }
@@ -211,12 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int N = (t.size + 15) & ~15;  // <= kMaxN
         const uint32_t idesc = idesc_bf16_f32(128, N);
         const int acc = it & 1;
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), ((it >> 1) & 1) ^ 1u, s_abort, p.err,
+        if (!mbar_wait_bounded<true>(smem_u32(&tempty[acc]), ((it >> 1) & 1) ^ 1u, s_abort, p.err,
                                ERR_TIMEOUT_MMA))
           break;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
+          if (!mbar_wait_bounded<true>(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0) {
         umma_commit(smem_u32(fin));
         volatile int no_abort = 0;
-        mbar_wait_bounded(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
+        mbar_wait_bounded<true>(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
       }
     }
   } else {
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = it & 1;
       int ok = 1;
       if (lane == 0)
-        ok = mbar_wait_bounded(smem_u32(&tfull[acc]), (it >> 1) & 1, s_abort, p.err,
+        ok = mbar_wait_bounded<true>(smem_u32(&tfull[acc]), (it >> 1) & 1, s_abort, p.err,
                                ERR_TIMEOUT_EPILOGUE);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
