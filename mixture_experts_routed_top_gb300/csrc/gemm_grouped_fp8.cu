@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int arow = s_off[e] + m * BM;
         const int brow = (EPI == EPI_SWIGLU_Q) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
+          if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) {
         if ((issued >> s) & 1u) {
           volatile int no_abort = 0;
-          mbar_wait_bounded(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
+          mbar_wait_bounded<true>(smem_u32(&full[s]), (last_par >> s) & 1u, &no_abort, p.err,
                             ERR_TIMEOUT_PRODUCER, 20000000ull);
         }
       }
@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < KB; ++kb, ++g) {
           const int b = g & 1;
           const uint32_t bph = (g >> 1) & 1;
-          if (!mbar_wait_bounded(smem_u32(&pempty[b]), bph ^ 1u, s_abort, p.err, ERR_TIMEOUT_MMA) ||
-              !mbar_wait_bounded(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
+          if (!mbar_wait_bounded<true>(smem_u32(&pempty[b]), bph ^ 1u, s_abort, p.err, ERR_TIMEOUT_MMA) ||
+              !mbar_wait_bounded<true>(smem_u32(&full[stage]), ph, s_abort, p.err, ERR_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g > 0) {
         umma_commit(smem_u32(fin));
         volatile int no_abort = 0;
-        mbar_wait_bounded(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
+        mbar_wait_bounded<true>(smem_u32(fin), 0, &no_abort, p.err, ERR_TIMEOUT_MMA);
       }
     }
   } else {
