@@ -8,7 +8,7 @@
 //   dispatch_small   one CTA: counts, scan, touched list, stable placement
 //   decode_gate_up   item = (touched expert, 4 features); warp = feature f:
 //                    gate and up rows of W_gate_up[e] streamed once, dotted
-//                    with the expert's token rows, h = silu(g) * u (bf16)
+//                    with the expert's token rows, h = act(g) * u (bf16)
 //   decode_down      item = (touched expert, 4 output columns); warp = one
 //                    row of W_down[e]; Y[r, c] = topk_w * (h[r] . W_down[e,c])
 //   decode_combine   out[t] = sum_j Y[row_of[t*k+j]] in fp32 -> bf16

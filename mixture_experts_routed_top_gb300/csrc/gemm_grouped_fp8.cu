@@ -6,7 +6,7 @@
 // block, so
 //     acc[r, c] = sum_kb s_a[r, kb] * s_w[c/128, kb] * (sum_{k in kb} qa[r,k] qw[c,k])
 // The tensor core computes each K-block's inner sum into a fresh TMEM buffer
-// (tcgen05.mma kind::f8f6f4, M=128, N=256, K=32 per instruction); two
+// (tcgen05.mma kind::f8f6f4, M=128, N=256, K=32 per instruction); four
 // epilogue warpgroups read it back and fold it into fp32 register
 // accumulators with the block's scale product.  Two 256-column TMEM buffers
 // let the MMA of K-block kb+1 run while K-block kb is being promoted.
@@ -18,7 +18,8 @@
 //                thread = tile row (TMEM lane), warpgroup = a quarter of the
 //                columns, so the per-K-block promotion is spread over 16 warps
 //     gate/up:   warpgroup g owns gate columns 32g..32g+31 and the matching up
-//                columns; at tile end h = silu(g)*u is re-quantised per row
+//                columns; at tile end h = act(g)*u (silu, exact GELU or
+//                relu) is re-quantised per row
 //                over the tile's 128 columns (one 1x128 block of I; the four
 //                warpgroups exchange their row maxima through shared memory)
 //     down:      warpgroup g owns output columns 64g..64g+63 (inside weight

@@ -1,5 +1,5 @@
 // Grouped tensor-core GEMMs (bf16), token-row orientation, for experts with
-// many routed rows (prefill).  The swap-AB kernel in gemm_grouped.cu covers
+// many routed rows (prefill).  The swap-AB kernel in gemm_swap.cu covers
 // experts with few rows.
 //
 // Rows of the activation matrix are expert-contiguous (the dispatch step);
@@ -17,7 +17,8 @@
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, thread = tile row
 //     gate/up GEMM:  B tile = 128 gate rows then the matching 128 up rows of
 //                    W_gate_up[e], so accumulator column j is gate and j+128
-//                    is up; h = silu(gate) * up stored as bf16
+//                    is up; h = act(gate) * up stored as bf16 (act: silu,
+//                    exact GELU or relu, uniform over the launch)
 //     down GEMM:     y scaled by the row's routing weight and added (fp32
 //                    vector atomics) into out32[token] - the combine
 // Every mbarrier wait is bounded; on expiry the kernel flags the error word,

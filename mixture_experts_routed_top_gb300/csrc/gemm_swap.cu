@@ -13,7 +13,8 @@
 //
 // Gate/up GEMM: box 0 = 128 gate rows, box 1 = the same 128 features' up
 //   rows; accumulators D0 (gate) and D1 (up) share TMEM lanes, so lane f
-//   holds gate and up of feature f: h[t, f] = silu(D0[f,t]) * D1[f,t].
+//   holds gate and up of feature f: h[t, f] = act(D0[f,t]) * D1[f,t] (act:
+//   silu, exact GELU or relu, uniform over the launch).
 // Down GEMM: boxes = 256 (or 128) consecutive rows of W_down[e]; the
 //   epilogue adds topk_w * D[f, t] into the fp32 accumulator row of the
 //   token (coalesced fp32 atomics across the warp's 32 features).

@@ -45,6 +45,33 @@ def test_weight_quantiser_bit_exact(moe, fmt):
         assert np.array_equal(s.cpu().numpy(), rs)
 
 
+@pytest.mark.parametrize("fmt", ["f32", "ue8m0"])
+def test_quantiser_every_bf16_value_at_scale_one(moe, fmt):
+    """Every finite bf16 value with |x| <= 448, through the device quantiser
+    (the hardware e4m3 conversion) at block scale exactly 1: each 128x128
+    block also holds 448, so amax = 448 and s = 448/448 = 1 (float32) or
+    2^0 (UE8M0).  The codes must be the oracle encoder's codes of the values
+    themselves, bit for bit."""
+    bits = np.arange(65536, dtype=np.uint32) << np.uint32(16)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= 448.0)]
+    per = 128 * 128 - 1
+    nblk = -(-vals.size // per)
+    arr = np.zeros((nblk, 128 * 128), np.float32)
+    arr[:, 0] = 448.0
+    for b in range(nblk):
+        chunk = vals[b * per:(b + 1) * per]
+        arr[b, 1:1 + chunk.size] = chunk
+    arr = arr.reshape(nblk, 128, 128)
+    q, sc = moe.quantize_fp8_blocks(torch.from_numpy(arr).to(torch.bfloat16).cuda(), fmt)
+    sc = sc.cpu().numpy()
+    if fmt == "f32":
+        assert np.all(sc == 1.0)
+    else:
+        assert np.all(sc == 127)
+    assert np.array_equal(q.cpu().numpy(), O.e4m3_encode(arr))
+
+
 def _fp8_case(moe, shape, fmt, seed=0, logit_bias=None, act="silu"):
     d = make_inputs(shape, seed=seed, device="cpu")
     logits = d["logits"] if logit_bias is None else d["logits"] + logit_bias
