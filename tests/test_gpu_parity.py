@@ -132,6 +132,7 @@ SMALL_SHAPES = [
     MoEShape(T=1, H=512, I=256, E=16, k=4),         # a single token
     MoEShape(T=40, H=1024, I=512, E=64, k=6),       # most experts get 1-10 rows
     MoEShape(T=3, H=128, I=128, E=2, k=2),          # k = E
+    MoEShape(T=64, H=128, I=128, E=1024, k=32),     # E and k at their limits, 2048 rows
 ]
 
 
