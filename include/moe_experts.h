@@ -187,8 +187,9 @@ moe_status moe_workspace_status(void* ws, void* stream);
  * moe_set_decode_rows - route bf16 forwards with T*k <= rows through the
  * small-token decode path (weight streaming over the touched experts only,
  * the page's "Decode-stage switching" idea); larger ones through the grouped
- * tensor-core path.  rows < 0 restores the default; values are clamped to
- * 2048 (the decode path's workspace is sized up to that many rows).
+ * tensor-core path.  rows < 0 restores the default (16, the measured
+ * crossover); values are clamped to 2048 (the decode path's workspace is
+ * sized up to that many rows).
  * Process-wide setting; moe_get_decode_rows returns the threshold in use.
  */
 void moe_set_decode_rows(int rows);
