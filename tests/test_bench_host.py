@@ -1,0 +1,57 @@
+"""Host-side arithmetic of bench.py that every reported roofline fraction
+depends on: algorithmic flops and bytes of a step, the peak table and the
+ncu traffic lookup.  CPU only."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import bench
+from workloads import shape_for
+
+
+def _w(name, T, wfmt="bf16", sfmt=None):
+    return {"shape": shape_for(name, T), "wfmt": wfmt, "sfmt": sfmt}
+
+
+def test_algorithmic_bf16_counts_routed_rows_and_touched_experts():
+    w = _w("qwen", 4096)
+    s = w["shape"]
+    counts = np.full(s.E, 4096 * 4 // s.E)
+    counts[7] = 0                                   # one expert untouched
+    flops, wbytes, io, touched = bench.algorithmic(w, counts)
+    assert flops == 6.0 * 2048 * 1408 * 4096 * 4    # 6 H I per routed row
+    assert touched == s.E - 1
+    assert wbytes == (s.E - 1) * 3 * 2048 * 1408 * 2
+    assert io == 4096 * 2048 * 2 * 2 + 4096 * 60 * 4
+
+
+@pytest.mark.parametrize("sfmt,per", [("f32", 4), ("ue8m0", 1)])
+def test_algorithmic_fp8_weight_bytes_include_block_scales(sfmt, per):
+    w = _w("dsv3_fp8", 64, "fp8", sfmt)
+    s = w["shape"]
+    counts = np.zeros(s.E, np.int64)
+    counts[:10] = 1
+    _, wbytes, _, touched = bench.algorithmic(w, counts)
+    scales = (2 * s.I // 128) * (s.H // 128) * per + (s.H // 128) * (s.I // 128) * per
+    assert touched == 10
+    assert wbytes == 10 * (3 * s.H * s.I + scales)
+
+
+def test_peaks_have_both_denominators():
+    peaks, src = bench.load_peaks()
+    assert src in ("measured", "fallback")
+    assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 100
+
+
+def test_traffic_lookup_follows_the_kernel_source():
+    assert bench.traffic_for("gemm1:no-such-workload") is None
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    for key, ent in d.items():
+        if key.startswith("_"):
+            continue
+        got = bench.traffic_for(key)
+        # either the kernel source still hashes as captured, or the entry is ignored
+        assert got in (None, ent["bytes_per_launch"])
+        assert ent["bytes_per_launch"] == ent["read"] + ent["write"]
