@@ -59,8 +59,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int g_decode_rows = -1;  // < 0: default
-int g_swap_rows = -1;    // < 0: default
+// Process-wide path thresholds (< 0: default); atomic, since any host
+// thread may set them while others launch forwards.
+std::atomic<int> g_decode_rows{-1};
+std::atomic<int> g_swap_rows{-1};
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -210,10 +212,16 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 void moe_set_decode_rows(int rows) {
   g_decode_rows = rows < 0 ? -1 : (rows > kDecodeRowsMax ? kDecodeRowsMax : rows);
 }
-int moe_get_decode_rows(void) { return g_decode_rows < 0 ? kDecodeRowsDefault : g_decode_rows; }
+int moe_get_decode_rows(void) {
+  const int r = g_decode_rows.load(std::memory_order_relaxed);
+  return r < 0 ? kDecodeRowsDefault : r;
+}
 
 void moe_set_swap_rows(int rows_per_expert) { g_swap_rows = rows_per_expert < 0 ? -1 : rows_per_expert; }
-int moe_get_swap_rows(void) { return g_swap_rows < 0 ? kSwapRowsDefault : g_swap_rows; }
+int moe_get_swap_rows(void) {
+  const int r = g_swap_rows.load(std::memory_order_relaxed);
+  return r < 0 ? kSwapRowsDefault : r;
+}
 
 moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                      void* stream) {
@@ -484,7 +492,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   // explicitly, which then applies to both (0: token rows always).
   const int swap_rows = moe_get_swap_rows();
   const bool swap1 = n <= static_cast<long>(swap_rows) * E;
-  const bool swap2 = g_swap_rows >= 0 ? swap1 : true;
+  const bool swap2 = g_swap_rows.load(std::memory_order_relaxed) >= 0 ? swap1 : true;
   // swap-AB kernel: 128-byte rows, token boxes of 64 rows; token-row
   // kernel: rows of kRowsBK bf16, 128-row boxes for both operands
   const uint32_t rb = kRowsBK * 2;
