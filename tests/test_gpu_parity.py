@@ -198,6 +198,36 @@ def test_forward_rejects_unknown_activation(moe):
         moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"], activation="tanh")
 
 
+def test_profile_read_after_graph_replays(moe):
+    """Stage events captured in a CUDA graph report each replay's stage
+    times through profile_read; eager profiling sums every launch."""
+    shape = MoEShape(T=256, H=256, I=256, E=8, k=2)
+    d = make_inputs(shape, seed=2, device="cuda")
+    idx, w = moe.route(d["logits"], shape.k)
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device="cuda")
+    ws = moe.Workspace("cuda")
+    run = lambda: moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"],
+                                      out=out, workspace=ws)
+    run()
+    torch.cuda.synchronize()
+    moe.profile_begin()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        st = moe.profile_read()
+        assert all(st[k][1] == 1 and st[k][0] > 0 for k in ("dispatch", "gemm1", "gemm2", "finish"))
+    moe.profile_end()
+    moe.profile_begin()
+    run()
+    run()
+    st = moe.profile_end()
+    assert st["gemm1"][1] == 2 and st["gemm2"][1] == 2
+    moe.workspace_status(ws)
+
+
 def test_all_paths_agree(moe):
     shape = MoEShape(T=96, H=512, I=384, E=16, k=4)
     d = make_inputs(shape, seed=5, device="cuda")
