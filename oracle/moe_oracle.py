@@ -54,6 +54,8 @@ __all__ = [
     "expert_mlp", "forward", "forward_brute", "round_to_bf16",
     "bf16_bits_to_f32", "e4m3_encode", "e4m3_decode", "ue8m0_from_quotient",
     "quantize_blocks", "dequantize_blocks", "forward_fp8",
+    "e2m1_encode", "e2m1_decode", "pack_e2m1", "unpack_e2m1", "quantize_fp4_blocks",
+    "dequantize_fp4_blocks", "forward_fp4",
     "touched_weight_bytes", "rel_max_err",
 ]
 
@@ -427,6 +429,132 @@ def forward_fp8(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down,
         if quantize_h:
             hq, _, hs = quantize_blocks(h.astype(np.float32), 1, 128, fmt)
             h = dequantize_blocks(hq, hs, 1, 128)
+        y = h @ wd[e].T
+        np.add.at(out, toks, w[toks, slots][:, None] * y)
+    return out
+
+
+# --------------------------------------------------------------------------
+# FP4 (e2m1) experts.  The page ("FP8 and FP4 quantized experts"; the
+# paragraph after the backends table) fixes only e2m1 codes packed in int8
+# with UE8M0 weight scales.  Readings: blocks of 1x32 along the contraction
+# axis (the MX convention; the page gives no size); scale = the smallest
+# power of two >= amax/6 (amax = 0 gives 1), as for FP8 with 6 in place of
+# 448; codes e2m1(x * (1/s)), round to nearest even, saturating to +-6; two
+# codes per byte, the even element in the low nibble.  The activations and
+# h of an FP4 forward are e4m3 with the same 1x32 UE8M0 blocks.
+# --------------------------------------------------------------------------
+
+E2M1_MAX = 6.0
+# magnitudes of the codes 0..7 (bit 3 is the sign): 0, then 2^(e-1)(1 + m/2)
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_decode(code: np.ndarray) -> np.ndarray:
+    """e2m1 codes (0..15, bit 3 = sign) -> float32 values."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    mag = _E2M1_MAG[c & 7]
+    return np.where(c & 8, -mag, mag).astype(np.float32)
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e2m1 codes (uint8 0..15): the nearest of the eight magnitudes,
+    ties to the even code (mantissa bit 0), magnitudes above 6 saturate to
+    6; the sign bit is x's sign bit (so -0.0 -> 8)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64)
+    hi = np.clip(np.searchsorted(_E2M1_MAG, a, side="left"), 1, 7)   # first magnitude >= a
+    lo = hi - 1
+    d_lo = a - _E2M1_MAG[lo]
+    d_hi = _E2M1_MAG[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    mag = np.where(pick_hi, hi, lo)
+    mag = np.where(a >= E2M1_MAX, 7, mag)
+    sign = (x.view(np.uint32) >> np.uint32(31)).astype(np.int64)
+    return (mag | (sign << 3)).astype(np.uint8)
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """codes [..., C] (C even) -> bytes [..., C/2], element 2i in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << np.uint8(4))).astype(np.uint8)
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    """bytes [..., C/2] -> codes [..., C]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & np.uint8(0xF)
+    out[..., 1::2] = p >> np.uint8(4)
+    return out
+
+
+def _ue8m0_block_scales(amax: np.ndarray, elem_max: float):
+    amax = np.asarray(amax, dtype=np.float32)
+    zero = amax == 0
+    q = (amax / np.float32(elem_max)).astype(np.float32)      # fp32 IEEE division
+    s, b = ue8m0_from_quotient(np.where(zero, np.float32(1.0), q))
+    s = np.where(zero, np.float32(1.0), s).astype(np.float32)
+    b = np.where(zero, np.uint8(127), b).astype(np.uint8)
+    return s, b
+
+
+def quantize_fp4_blocks(x: np.ndarray, block: int = 32):
+    """x [..., C] (float32 values) -> (packed e2m1 bytes [..., C/2], UE8M0
+    exponent bytes [..., C/block], scale values float32 [..., C/block])."""
+    x = np.asarray(x, dtype=np.float32)
+    *lead, C = x.shape
+    if C % block or block % 2:
+        raise ValueError("last axis not divisible by the block size")
+    xb = x.reshape(*lead, C // block, block)
+    s, b = _ue8m0_block_scales(np.abs(xb).max(axis=-1), E2M1_MAX)
+    y = (xb * (np.float32(1.0) / s)[..., None]).astype(np.float32)   # exact: s is 2^j
+    codes = e2m1_encode(y).reshape(*lead, C)
+    return pack_e2m1(codes), b, s
+
+
+def dequantize_fp4_blocks(packed: np.ndarray, scales: np.ndarray, block: int = 32,
+                          dtype=np.float64) -> np.ndarray:
+    """packed e2m1 bytes [..., C/2] with scale values [..., C/block] -> values."""
+    v = e2m1_decode(unpack_e2m1(packed)).astype(dtype)
+    return v * np.repeat(np.asarray(scales, dtype=dtype), block, axis=-1)
+
+
+def _e4m3_rows_1xb(x: np.ndarray, block: int) -> np.ndarray:
+    """Dynamic e4m3 quantisation of rows in 1 x block UE8M0 blocks, dequantised."""
+    q, _, s = quantize_blocks(np.asarray(x, dtype=np.float32), 1, block, "ue8m0")
+    return dequantize_blocks(q, s, 1, block)
+
+
+def forward_fp4(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down, ws_down,
+                block: int = 32, quantize_act: bool = True, quantize_h: bool = True,
+                act: str = "silu") -> np.ndarray:
+    """FP4-weight forward, mirrored: weights are packed e2m1 [E, 2I, H/2] and
+    [E, H, I/2] with UE8M0 exponent bytes [E, 2I, H/block] and [E, H, I/block];
+    the hidden rows and h are quantised to e4m3 in 1 x block UE8M0 blocks;
+    math in float64 otherwise.  Returns the un-rounded output [T,H]."""
+    T, H = hidden.shape
+    E = wq_gate_up.shape[0]
+    k = topk_idx.shape[1]
+    I = wq_gate_up.shape[1] // 2
+    wgu = dequantize_fp4_blocks(wq_gate_up, scale_values(ws_gate_up, "ue8m0"), block)
+    wd = dequantize_fp4_blocks(wq_down, scale_values(ws_down, "ue8m0"), block)
+    counts, offsets, sorted_f, _ = dispatch(topk_idx, E)
+    w = np.asarray(topk_w, dtype=np.float64)
+    out = np.zeros((T, H), dtype=np.float64)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        rows = sorted_f[offsets[e]:offsets[e + 1]].astype(np.int64)
+        toks = rows // k
+        slots = rows % k
+        x = np.asarray(hidden[toks], dtype=np.float32)
+        x = _e4m3_rows_1xb(x, block) if quantize_act else x.astype(np.float64)
+        g = x @ wgu[e, :I].T
+        u = x @ wgu[e, I:].T
+        h = ACTIVATIONS[act](g) * u
+        if quantize_h:
+            h = _e4m3_rows_1xb(h, block)
         y = h @ wd[e].T
         np.add.at(out, toks, w[toks, slots][:, None] * y)
     return out

@@ -381,3 +381,93 @@ def test_fp8_forward_close_to_bf16_forward():
         out = O.forward_fp8(hidden, idx, w, qgu, sgu, qd, sd, fmt)
         rel_rms = np.sqrt(np.mean((out - ref) ** 2) / np.mean(ref ** 2))
         assert rel_rms < 0.25, rel_rms
+
+
+# --------------------------------------------------------------------------
+# FP4 (e2m1) experts: the oracle parts written ahead of their kernel
+# --------------------------------------------------------------------------
+
+def test_e2m1_code_table_closed_form():
+    """Code s|e e|m: (-1)^s * m/2 for e = 0, else (-1)^s * 2^(e-1) * (1 + m/2)."""
+    c = np.arange(16, dtype=np.uint8)
+    e = (c.astype(np.int64) >> 1) & 3
+    m = c.astype(np.int64) & 1
+    mag = np.where(e == 0, m / 2.0, np.ldexp(1.0 + m / 2.0, e - 1))
+    ref = np.where(c & 8, -mag, mag)
+    np.testing.assert_array_equal(O.e2m1_decode(c), ref.astype(np.float32))
+    np.testing.assert_array_equal(O.e2m1_encode(O.e2m1_decode(c)), c)
+
+
+def test_e2m1_ties_to_even_and_saturation():
+    x = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 1e9, -0.0, -5.5, 0.2, 0.3],
+                 np.float32)
+    want = np.array([0, 2, 2, 4, 4, 6, 6, 7, 7, 8, 15, 0, 1], np.uint8)
+    np.testing.assert_array_equal(O.e2m1_encode(x), want)
+
+
+def test_e2m1_nearest_value_brute_force():
+    x = np.random.default_rng(9).uniform(-7.0, 7.0, 200000).astype(np.float32)
+    got = O.e2m1_decode(O.e2m1_encode(x)).astype(np.float64)
+    grid = O.e2m1_decode(np.arange(8, dtype=np.uint8)).astype(np.float64)
+    a = np.minimum(np.abs(x.astype(np.float64)), 6.0)
+    best = np.abs(a[:, None] - grid[None, :]).min(axis=1)
+    assert np.all(np.abs(np.abs(got) - a) == best)
+    assert np.all((got == 0) | (np.sign(got) == np.sign(x)))
+
+
+def test_e2m1_matches_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    if not hasattr(ml, "float4_e2m1fn"):
+        pytest.skip("ml_dtypes without float4_e2m1fn")
+    # every fp32 pattern with |x| in [2^-4, 2^4), both signs, thinned 1:64
+    bits = np.arange((127 - 4) << 23, (127 + 4) << 23, 64, dtype=np.uint32)
+    for sgn in (0, 0x80000000):
+        x = (bits | np.uint32(sgn)).view(np.float32)
+        ref = np.asarray(x.astype(ml.float4_e2m1fn)).view(np.uint8) & 0xF
+        np.testing.assert_array_equal(O.e2m1_encode(x), ref)
+
+
+def test_fp4_pack_unpack_round_trip():
+    c = np.random.default_rng(3).integers(0, 16, size=(5, 64)).astype(np.uint8)
+    p = O.pack_e2m1(c)
+    assert p.shape == (5, 32)
+    np.testing.assert_array_equal(p[:, 0] & 0xF, c[:, 0])
+    np.testing.assert_array_equal(p[:, 0] >> 4, c[:, 1])
+    np.testing.assert_array_equal(O.unpack_e2m1(p), c)
+
+
+def test_fp4_block_quantiser_bounds():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((6, 256)) * np.exp(rng.uniform(-8, 8, (6, 1)))).astype(np.float32)
+    x[2, 32:64] = 0.0                                     # an all-zero block
+    packed, stored, s = O.quantize_fp4_blocks(x, 32)
+    assert packed.shape == (6, 128) and stored.shape == (6, 8)
+    np.testing.assert_array_equal(O.scale_values(stored, "ue8m0"), s)
+    amax = np.abs(x.reshape(6, 8, 32)).max(axis=-1)
+    nz = amax > 0
+    assert np.all(np.frexp(s)[0] == 0.5)                 # powers of two
+    assert np.all(s[nz] >= amax[nz] / 6.0) and np.all(s[nz] < 2.0 * amax[nz] / 6.0)
+    assert s[2, 1] == 1.0 and stored[2, 1] == 127
+    deq = O.dequantize_fp4_blocks(packed, s, 32)
+    # error within half the widest spacing (2) of the grid at the block scale
+    err = np.abs(deq - x.astype(np.float64)).reshape(6, 8, 32).max(axis=-1)
+    assert np.all(err <= 1.0 * s + 1e-30)
+
+
+def test_fp4_forward_without_act_quant_is_bf16_oracle_on_dequantised_weights():
+    shape = MoEShape(T=20, H=128, I=64, E=4, k=2)
+    logits, hidden, wgu, wd = _np_inputs(shape)
+    idx, w = O.route(logits, 2)
+    qgu, bgu, _ = O.quantize_fp4_blocks(wgu, 32)
+    qd, bd, _ = O.quantize_fp4_blocks(wd, 32)
+    out4 = O.forward_fp4(hidden, idx, w, qgu, bgu, qd, bd, 32,
+                         quantize_act=False, quantize_h=False, act="silu")
+    ref = O.forward(hidden, idx, w, O.dequantize_fp4_blocks(qgu, O.scale_values(bgu, "ue8m0")),
+                    O.dequantize_fp4_blocks(qd, O.scale_values(bd, "ue8m0")))
+    np.testing.assert_allclose(out4, ref, rtol=1e-12, atol=1e-14)
+    # with the activations and h quantised it stays near the bf16 forward:
+    # e2m1 carries ~10-20 % relative error per weight, so the rms error of
+    # the output is a fraction of its rms
+    q = O.forward_fp4(hidden, idx, w, qgu, bgu, qd, bd, 32)
+    ref32 = O.forward(hidden, idx, w, wgu, wd)
+    assert np.sqrt(np.mean((q - ref32) ** 2)) < 0.5 * np.sqrt(np.mean(ref32 ** 2))
