@@ -52,6 +52,11 @@ WORKLOADS = {
     # profiling-sized layers (32 experts), used for ncu captures
     "dsv3e32-fp8-2048-f32": ("dsv3_e32", 2048, "fp8", "f32"),
     "dsv3e32-fp8-8-f32": ("dsv3_e32", 8, "fp8", "f32"),
+    # FP4 (e2m1, 1x32 UE8M0 blocks) experts: small-token batches only
+    "qwen-fp4-decode-1": ("qwen", 1, "fp4", "ue8m0"),
+    "qwen-fp4-decode-16": ("qwen", 16, "fp4", "ue8m0"),
+    "dsv3-fp4-1": ("dsv3", 1, "fp4", "ue8m0"),
+    "dsv3-fp4-8": ("dsv3", 8, "fp4", "ue8m0"),
 }
 DESCRIPTIONS = {
     "qwen": "Qwen1.5-MoE-A2.7B-shaped MoE layer",
@@ -61,6 +66,15 @@ DESCRIPTIONS = {
     "dsv3_e32": "DeepSeek-V3-width MoE layer with 32 experts (profiling size), e4m3 weights",
 }
 L2_BYTES = 129 * 2 ** 20
+BYTES_PER_WEIGHT = {"bf16": 2.0, "fp8": 1.0, "fp4": 0.5}
+WDTYPE = {"bf16": 0, "fp8": 1, "fp4": 2}
+DTYPE_NAME = {"bf16": "bf16", "fp8": "fp8-e4m3", "fp4": "fp4-e2m1"}
+
+
+def describe(name):
+    sname, _, wfmt, _ = WORKLOADS[name]
+    d = DESCRIPTIONS[sname]
+    return d + ", packed e2m1 weights with 1x32 UE8M0 scales" if wfmt == "fp4" else d
 
 
 def log(*a):
@@ -180,11 +194,15 @@ def build_workload(name, device):
         w["q_gate_up"], w["s_gate_up"] = moe.quantize_fp8_blocks(d["w_gate_up"], sfmt)
         w["q_down"], w["s_down"] = moe.quantize_fp8_blocks(d["w_down"], sfmt)
         torch.cuda.synchronize()
+    elif wfmt == "fp4":
+        w["q_gate_up"], w["s_gate_up"] = moe.quantize_fp4_blocks(d["w_gate_up"])
+        w["q_down"], w["s_down"] = moe.quantize_fp4_blocks(d["w_down"])
+        torch.cuda.synchronize()
     return w
 
 
 def weights_of(w):
-    if w["wfmt"] == "fp8":
+    if w["wfmt"] in ("fp8", "fp4"):
         return dict(w_gate_up=w["q_gate_up"], w_down=w["q_down"], scale_gate_up=w["s_gate_up"],
                     scale_down=w["s_down"], scale_fmt=w["sfmt"])
     return dict(w_gate_up=w["w_gate_up"], w_down=w["w_down"])
@@ -196,12 +214,14 @@ def algorithmic(w, counts):
     s = w["shape"]
     rows = s.T * s.k
     flops = 6.0 * s.H * s.I * rows
-    bpw = 1.0 if w["wfmt"] == "fp8" else 2.0
+    bpw = BYTES_PER_WEIGHT[w["wfmt"]]
     touched = int((counts > 0).sum())
     scale_b = 0
     if w["wfmt"] == "fp8":
         per = 4 if w["sfmt"] == "f32" else 1
         scale_b = (2 * s.I // 128) * (s.H // 128) * per + (s.H // 128) * (s.I // 128) * per
+    elif w["wfmt"] == "fp4":   # one UE8M0 byte per 32 weights
+        scale_b = 2 * s.I * (s.H // 32) + s.H * (s.I // 32)
     wbytes = touched * (3.0 * s.H * s.I * bpw + scale_b)
     io = s.T * s.H * 2 * 2 + s.T * s.E * 4
     return flops, wbytes, io, touched
@@ -262,7 +282,7 @@ class OracleSample:
             ex = new
         toks, ex = np.array(toks), sorted(ex)
         et = torch.tensor(ex, device=w["hidden"].device)
-        if w["wfmt"] == "fp8":
+        if w["wfmt"] in ("fp8", "fp4"):
             self.parts = [w["q_gate_up"].index_select(0, et).cpu().numpy(),
                           w["s_gate_up"].index_select(0, et).cpu().numpy(),
                           w["q_down"].index_select(0, et).cpu().numpy(),
@@ -285,6 +305,8 @@ class OracleSample:
         act = self.w.get("act", "silu")
         if self.w["wfmt"] == "fp8":
             O.forward_fp8(self.hid, lidx, wt, *self.parts, self.w["sfmt"], act=act)
+        elif self.w["wfmt"] == "fp4":
+            O.forward_fp4(self.hid, lidx, wt, *self.parts, act=act)
         else:
             O.forward(self.hid, lidx, wt, *self.parts, act=act)
         return time.perf_counter() - t0
@@ -335,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
     moe.workspace_status(ws)
     counts = torch.bincount(idx.flatten().long(), minlength=s.E).cpu().numpy()
     flops, wbytes, io_bytes, touched = algorithmic(w, counts)
-    ws_bytes = moe.workspace_size(s.T, s.H, s.I, s.E, s.k, 1 if w["wfmt"] == "fp8" else 0)
+    ws_bytes = moe.workspace_size(s.T, s.H, s.I, s.E, s.k, WDTYPE[w["wfmt"]])
     working_set = wbytes + io_bytes
     flush = working_set < 2 * L2_BYTES
     flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
@@ -528,7 +550,6 @@ def run_ours(args, rank, world, local_rank):
     tok_s = job_throughput(s.T, args.steps, world, total_ms)
     g1_ms, g1_n = stages["gemm1"]
     g2_ms, g2_n = stages["gemm2"]
-    bytes_per_w = 1.0 if w["wfmt"] == "fp8" else 2.0
     dominant = "gemm1" if g1_ms >= g2_ms else "gemm2"
     d_ms, d_n = stages[dominant]
     d_avg_s = d_ms / max(d_n, 1) / 1e3
@@ -548,7 +569,17 @@ def run_ours(args, rank, world, local_rank):
     peak_kind = ("hbm_gbs, STREAM-style copy" if hbm_bound else
                  "bf16 burst" if w["wfmt"] == "bf16" else "bf16 burst x2 nominal fp8/bf16 ratio")
     # the same kernel against the other roof (both matter near the ridge)
-    if hbm_bound:
+    if w["wfmt"] == "fp4":
+        # the FP4 GEMVs run their multiply-adds on CUDA cores: fp32 FMA peak
+        # = SMs x 128 lanes x 2 flops x the largest SM clock seen
+        props = torch.cuda.get_device_properties(dev)
+        clk_max = (clk.summary() or {}).get("sm_max_mhz") or 2070
+        pk_a = props.multi_processor_count * 128 * 2 * float(clk_max) * 1e6 / 1e12
+        a_a = kern_flops / d_avg_s / 1e12
+        roof_other = {"bound": "alu", "achieved": round(a_a, 2), "peak": round(pk_a, 1),
+                      "unit": "TFLOP/s", "frac": round(a_a / pk_a, 4),
+                      "peak_source": "fp32 FMA on CUDA cores, SM count x 128 x 2 x max SM clock"}
+    elif hbm_bound:
         pk_t = peaks["bf16_tflops"] * (2.0 if w["wfmt"] == "fp8" else 1.0)
         a_t = kern_flops / d_avg_s / 1e12
         roof_other = {"bound": "tensor", "achieved": round(a_t, 1), "peak": pk_t,
@@ -573,8 +604,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3" if w["wfmt"] == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "description": DESCRIPTIONS[WORKLOADS[args.workload][0]],
+        "dtype": DTYPE_NAME[w["wfmt"]], "data": "synthetic",
+        "config": {"workload": args.workload, "description": describe(args.workload),
                    "T": s.T, "H": s.H, "I": s.I, "E": s.E, "k": s.k,
                    "scale_fmt": w["sfmt"], "parallelism": f"replicas x{world}",
                    "l2": ("flushed before every timed step (512 MB write)" if flush else
@@ -663,9 +694,9 @@ def run_reference(args):
     each step is the same bounded sample of the workload."""
     import torch
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    if WORKLOADS[args.workload][2] == "fp8" and dev.type != "cuda":
+    if WORKLOADS[args.workload][2] in ("fp8", "fp4") and dev.type != "cuda":
         print(json.dumps({"impl": "reference",
-                          "unavailable": "the fp8 workload builds its weights with the GPU quantiser"}))
+                          "unavailable": "the quantised workload builds its weights with the GPU quantiser"}))
         return 0
     w = build_workload(args.workload, dev)
     w["act"] = args.activation
@@ -681,7 +712,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": args.workload,
-                       "description": DESCRIPTIONS[WORKLOADS[args.workload][0]],
+                       "description": describe(args.workload),
                        "T": s.T, "H": s.H, "I": s.I, "E": s.E, "k": s.k,
                        "scale_fmt": w["sfmt"], "activation": args.activation},
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",

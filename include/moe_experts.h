@@ -10,8 +10,9 @@
  * summed with the routing weights.  Tokens are ordered by selected expert
  * before the expert GEMMs (backends table, grouped_mm and deepgemm rows).  FP8
  * experts carry float32 or UE8M0 block scales (paragraph after the backends
- * table) and activations are quantised dynamically per row ("FP8 and FP4
- * quantized experts" section).
+ * table), FP4 experts are int8-packed e2m1 codes with UE8M0 scales, and
+ * activations are quantised dynamically per row ("FP8 and FP4 quantized
+ * experts" section).
  *
  * Conventions shared by every entry point:
  *   - All pointers named as device buffers must point to device memory of the
@@ -47,7 +48,7 @@ typedef enum {
   MOE_ERR_WORKSPACE = 5     /* workspace missing or smaller than required     */
 } moe_status;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1 } moe_wdtype;
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_FP4_E2M1 = 2 } moe_wdtype;
 
 /* Block-scale format of FP8 weights (and of the dynamic activation scales,
  * which always use the weights' format): MOE_SCALE_F32 stores float32 scales,
@@ -114,6 +115,14 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
  *               activations (hidden rows and the SwiGLU output) are quantised
  *               on the fly per row in 1x128 blocks with the same format.
  *               There is no static activation scale.
+ *               MOE_W_FP4_E2M1: weights are e2m1 codes packed two per byte,
+ *               the even element in the low nibble: w_gate_up [E, 2I, H/2],
+ *               w_down [E, H, I/2] bytes, with one UE8M0 byte per 1x32 block
+ *               along the contraction axis: scale_gate_up [E, 2I, H/32],
+ *               scale_down [E, H, I/32]; sfmt must be MOE_SCALE_UE8M0.  The
+ *               hidden rows and the SwiGLU output are quantised on the fly to
+ *               e4m3 in 1x32 UE8M0 blocks.  Only the small-token path exists
+ *               for this format: T*k <= 64, else MOE_ERR_UNSUPPORTED.
  *   out         device bf16 [T, H]: out[t] = sum_j topk_w[t,j] *
  *               down(silu(gate x_t) * up x_t) of expert topk_idx[t,j],
  *               accumulated in fp32 and rounded once to bf16
@@ -121,7 +130,8 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
  * Requirements: H % 128 == 0 (H % 256 == 0 for FP8 weights), I % 128 == 0,
  * 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 is a no-op).  Other
  * shapes: MOE_ERR_UNSUPPORTED.
- * FP8 weights with MOE_SCALE_NONE: MOE_ERR_INVALID_ARG.
+ * FP8 weights with MOE_SCALE_NONE, FP4 weights without MOE_SCALE_UE8M0:
+ * MOE_ERR_INVALID_ARG.
  * Inputs are never written; out is fully overwritten.
  * Calls that share one ws must be ordered (same stream or synchronised).
  */
@@ -173,6 +183,22 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H,
 moe_status moe_quantize_fp8_blocks(const void* w, int nmat, int rows, int cols,
                                    moe_scale_fmt sfmt, uint8_t* q, void* scale,
                                    void* stream);
+
+/*
+ * moe_quantize_fp4_blocks - quantise bf16 matrices into packed e2m1 codes
+ * with one UE8M0 scale per 1x32 block along each row (the FP4 expert format
+ * of the "FP8 and FP4 quantized experts" section).  Scale s = the smallest
+ * power of two >= amax/6 (float32 division; amax = 0 gives s = 1), stored
+ * as the biased exponent byte b, s = 2^(b-127); code = the e2m1 value
+ * nearest to x * (1/s) (0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives),
+ * ties to the even code, saturated to +-6; two codes per byte, the even
+ * element in the low nibble.  Inputs must be finite.
+ *   w      device bf16 [nmat, rows, cols], cols % 32 == 0
+ *   q      device uint8 [nmat, rows, cols/2]
+ *   scale  device uint8 [nmat, rows, cols/32]
+ */
+moe_status moe_quantize_fp4_blocks(const void* w, int nmat, int rows, int cols,
+                                   uint8_t* q, uint8_t* scale, void* stream);
 
 /*
  * moe_workspace_status - synchronise `stream`, read and clear the device

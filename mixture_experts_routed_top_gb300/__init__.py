@@ -18,17 +18,17 @@ from . import build as _build
 
 __all__ = [
     "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
-    "experts_forward", "quantize_fp8_blocks", "workspace_status", "set_decode_rows",
+    "experts_forward", "quantize_fp8_blocks", "quantize_fp4_blocks", "workspace_status", "set_decode_rows",
     "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
     "selftest_wait_timeout", "launch_count",
-    "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "SCALE_NONE", "SCALE_F32",
+    "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "W_FP4_E2M1", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0", "ACTIVATIONS",
 ]
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_WORKSPACE"}
 STAGES = ("dispatch", "gemm1", "gemm2", "finish")
-W_BF16, W_FP8_E4M3 = 0, 1
+W_BF16, W_FP8_E4M3, W_FP4_E2M1 = 0, 1, 2
 SCALE_NONE, SCALE_F32, SCALE_UE8M0 = 0, 1, 2
 _SCALE_BY_NAME = {None: SCALE_NONE, "none": SCALE_NONE, "f32": SCALE_F32, "float": SCALE_F32,
                   "ue8m0": SCALE_UE8M0}
@@ -54,6 +54,7 @@ _SIGS = {
     "moe_experts_forward_act": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _P,
                                  _P, _SZ, _P], _I),
     "moe_quantize_fp8_blocks": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_quantize_fp4_blocks": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_workspace_status": ([_P, _P], _I),
     "moe_set_decode_rows": ([_I], None),
     "moe_get_decode_rows": ([], _I),
@@ -182,22 +183,29 @@ def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.
 
     hidden bf16 [T,H]; topk_idx int32 [T,k]; topk_w fp32 [T,k];
     w_gate_up [E,2I,H] and w_down [E,H,I], bf16 or e4m3 bytes (uint8 or
-    float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0');
-    activation: the gate activation, 'silu' (SwiGLU), 'gelu' (GeGLU, exact
+    float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0'),
+    or packed e2m1 bytes (uint8 or int8) [E,2I,H/2] and [E,H,I/2] with 1x32
+    UE8M0 scales from quantize_fp4_blocks (T*k <= 64 only); activation: the gate activation, 'silu' (SwiGLU), 'gelu' (GeGLU, exact
     erf GELU) or 'relu' (ReGLU)."""
     _need_cuda(hidden, topk_idx, topk_w, w_gate_up, w_down, scale_gate_up, scale_down, out)
     T, H = hidden.shape
     k = topk_idx.shape[1]
     E, twoI, H2 = w_gate_up.shape
     I = twoI // 2
-    if H2 != H or tuple(w_down.shape) != (E, H, I):
+    fp4 = w_gate_up.dtype in (torch.uint8, torch.int8) and 2 * H2 == H
+    if fp4:
+        if tuple(w_down.shape) != (E, H, I // 2):
+            raise ValueError("packed FP4 weight shapes must be [E, 2I, H/2] and [E, H, I/2]")
+        if scale_fmt is None:
+            scale_fmt = "ue8m0"
+    elif H2 != H or tuple(w_down.shape) != (E, H, I):
         raise ValueError("weight shapes must be [E, 2I, H] and [E, H, I]")
     if hidden.dtype != torch.bfloat16 or topk_idx.dtype != torch.int32 or topk_w.dtype != torch.float32:
         raise ValueError("hidden bf16, topk_idx int32, topk_w fp32 expected")
-    fp8 = w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
-    wdtype = W_FP8_E4M3 if fp8 else W_BF16
-    if not fp8 and w_gate_up.dtype != torch.bfloat16:
-        raise ValueError("weights must be bf16 or e4m3 bytes")
+    fp8 = not fp4 and w_gate_up.dtype in (torch.uint8, torch.float8_e4m3fn)
+    wdtype = W_FP4_E2M1 if fp4 else W_FP8_E4M3 if fp8 else W_BF16
+    if not (fp4 or fp8) and w_gate_up.dtype != torch.bfloat16:
+        raise ValueError("weights must be bf16, e4m3 bytes or packed e2m1 bytes")
     sf = _SCALE_BY_NAME[scale_fmt] if not isinstance(scale_fmt, int) else scale_fmt
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
@@ -248,6 +256,23 @@ def quantize_fp8_blocks(w: torch.Tensor, scale_fmt: str = "f32", stream=None):
                     dtype=sdt, device=w.device)
     _check(lib().moe_quantize_fp8_blocks(_ptr(w), nmat, R, C, sf, _ptr(q), _ptr(s),
                                          _stream(stream)))
+    return q, s
+
+
+def quantize_fp4_blocks(w: torch.Tensor, stream=None):
+    """bf16 [..., R, C] -> (packed e2m1 codes uint8 [..., R, C/2], two per
+    byte with the even element in the low nibble; UE8M0 exponent bytes
+    uint8 [..., R, C/32], one per 1x32 block)."""
+    _need_cuda(w)
+    if w.dtype != torch.bfloat16:
+        raise ValueError("w must be bf16")
+    *lead, R, C = w.shape
+    nmat = 1
+    for d in lead:
+        nmat *= d
+    q = torch.empty(*lead, R, C // 2, dtype=torch.uint8, device=w.device)
+    s = torch.empty(*lead, R, C // 32, dtype=torch.uint8, device=w.device)
+    _check(lib().moe_quantize_fp4_blocks(_ptr(w), nmat, R, C, _ptr(q), _ptr(s), _stream(stream)))
     return q, s
 
 

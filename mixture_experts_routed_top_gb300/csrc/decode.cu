@@ -14,8 +14,7 @@
 //   decode_combine   out[t] = sum_j Y[row_of[t*k+j]] in fp32 -> bf16
 // Work items are spread over a persistent grid (grid-stride), so every SM
 // streams weights whatever the number of touched experts.
-#include "moe_device.cuh"
-#include "moe_internal.h"
+#include "decode_common.cuh"
 
 namespace moe {
 
@@ -81,10 +80,6 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
 }
 
 // ------------------------------------------------------------ helpers
-// Weights are read once: cache-streaming loads, which the compiler can
-// batch ahead of the arithmetic that consumes them.
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -92,12 +87,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
-}
-
-__device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8], float acc) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
-  return acc;
 }
 
 constexpr int kStreamBatch = 8;  // 16-byte weight vectors per lane loaded before any math
@@ -163,12 +152,6 @@ __device__ __forceinline__ void stream_dot1(const uint4* __restrict__ w,
       }
     }
   }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
 }
 
 // ------------------------------------------------------------ gate/up
@@ -285,53 +268,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __res
 // shared memory (stable order by expert, touched list), so no dispatch
 // kernel runs; the down GEMV also sums the k contributions of each token in
 // place, so no combine kernel runs either.
-struct SmallTable {
-  int sf[kFusedDecodeRows];       // row r -> flat entry f (stable, by expert)
-  int te[kFusedDecodeRows];       // touched experts, ascending
-  int tb[kFusedDecodeRows + 1];   // first row of each touched expert (+ end)
-  int nt;                         // number of touched experts
-  int idx[kFusedDecodeRows];
-};
-
-// All threads of the block call this; blockDim.x >= n.
-__device__ void build_small_table(const int32_t* __restrict__ topk_idx, int n, int E,
-                                  SmallTable& t, int* err) {
-  const int tid = threadIdx.x;
-  if (tid < n) t.idx[tid] = __ldg(topk_idx + tid);
-  __syncthreads();
-  if (tid < n) {
-    const int e = t.idx[tid];
-    if (e >= 0 && e < E) {
-      int rank = 0;
-      for (int f2 = 0; f2 < n; ++f2) {
-        const int e2 = t.idx[f2];
-        rank += (e2 >= 0 && e2 < E) && (e2 < e || (e2 == e && f2 < tid));
-      }
-      t.sf[rank] = tid;
-    } else if (blockIdx.x == 0) {
-      atomicOr(err, ERR_BAD_INDEX);
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int nv = 0;
-    for (int f = 0; f < n; ++f) nv += t.idx[f] >= 0 && t.idx[f] < E;
-    int nt = 0, prev = -1;
-    for (int r = 0; r < nv; ++r) {
-      const int e = t.idx[t.sf[r]];
-      if (e != prev) {
-        t.te[nt] = e;
-        t.tb[nt] = r;
-        ++nt;
-        prev = e;
-      }
-    }
-    t.tb[nt] = nv;
-    t.nt = nt;
-  }
-  __syncthreads();
-}
-
 template <int MT>
 __global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
     const __nv_bfloat16* __restrict__ hidden, int H, int I, int k, int E, int n,

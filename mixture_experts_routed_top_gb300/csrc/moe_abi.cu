@@ -71,8 +71,10 @@ struct WsLayout {
   size_t total;
 };
 
-WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
+WsLayout ws_layout(long T, long H, long I, long E, long k, moe_wdtype wd) {
   WsLayout L{};
+  const bool fp8 = wd == MOE_W_FP8_E4M3;
+  const bool fp4 = wd == MOE_W_FP4_E2M1;
   const long n = T * k;
   const long nchunks = n ? (n + dispatch_chunk(n) - 1) / dispatch_chunk(n) : 0;
   size_t off = sizeof(WsHeader);
@@ -88,8 +90,10 @@ WsLayout ws_layout(long T, long H, long I, long E, long k, bool fp8) {
   L.sorted_f = take(n * 4);
   L.row_of = take(n * 4);
   L.blk_counts = take(nchunks * E * 4);
-  const size_t esz = fp8 ? 1 : 2;
-  L.xa = take(n * H * esz);
+  // activations and h: e4m3 codes (FP8), bf16, or the quantised values in
+  // fp32 (FP4, which keeps one row per token for the activations)
+  const size_t esz = fp8 ? 1 : fp4 ? 4 : 2;
+  L.xa = take((fp4 ? T : n) * H * esz);
   L.xa_scale = take(fp8 ? n * scale_stride(H / 128) * 4 : 0);
   L.hb = take(n * I * esz);
   L.hb_scale = take(fp8 ? n * scale_stride(I / 128) * 4 : 0);
@@ -280,7 +284,7 @@ moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, int32_t* c
 
 size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
-  return ws_layout(T, H, I, E, k, wdtype == MOE_W_FP8_E4M3).total;
+  return ws_layout(T, H, I, E, k, wdtype).total;
 }
 
 moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* topk_idx,
@@ -313,7 +317,8 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   if (static_cast<long>(T) * k > 0x7FFFFFFFL)
     return fail(MOE_ERR_UNSUPPORTED, "moe_experts_forward: T*k exceeds int32");
   const bool fp8 = wdtype == MOE_W_FP8_E4M3;
-  if (wdtype != MOE_W_BF16 && !fp8)
+  const bool fp4 = wdtype == MOE_W_FP4_E2M1;
+  if (wdtype != MOE_W_BF16 && !fp8 && !fp4)
     return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: unknown weight dtype %d", (int)wdtype);
   if (fp8) {
     if (sfmt != MOE_SCALE_F32 && sfmt != MOE_SCALE_UE8M0)
@@ -321,6 +326,15 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
                   "moe_experts_forward: FP8 weights need float32 or UE8M0 block scales");
     if (!scale_gate_up || !scale_down)
       return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP8 weights need scale buffers");
+  } else if (fp4) {
+    if (sfmt != MOE_SCALE_UE8M0)
+      return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need UE8M0 block scales");
+    if (!scale_gate_up || !scale_down)
+      return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need scale buffers");
+    if (static_cast<long>(T) * k > kFusedDecodeRows)
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "moe_experts_forward: FP4 weights run on the small-token path only (T*k <= %d)",
+                  kFusedDecodeRows);
   } else if (sfmt != MOE_SCALE_NONE || scale_gate_up || scale_down) {
     return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: bf16 weights take no scales");
   }
@@ -332,7 +346,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     if (!aligned(q, 16)) return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: buffers must be 16-byte aligned");
   if (!aligned(ws, 256))
     return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: ws must be 256-byte aligned");
-  const WsLayout L = ws_layout(T, H, I, E, k, fp8);
+  const WsLayout L = ws_layout(T, H, I, E, k, wdtype);
   if (ws_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE, "moe_experts_forward: workspace %zu < %zu bytes", ws_bytes,
                 L.total);
@@ -358,6 +372,42 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
 
   const int sms = num_sms();
   cudaError_t e;
+  if (fp4) {
+    // packed e2m1 weights, small-token path: the routing table is rebuilt
+    // in the gate/up and down kernels, and the down kernel combines
+    Fp4DecodeArgs a;
+    a.hidden = hidden;
+    a.w_gate_up = w_gate_up;
+    a.w_down = w_down;
+    a.scale_gate_up = scale_gate_up;
+    a.scale_down = scale_down;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.xdq = reinterpret_cast<float*>(w + L.xa);
+    a.hq = reinterpret_cast<float*>(w + L.hb);
+    a.out = out;
+    a.err = d.err;
+    a.T = T;
+    a.H = H;
+    a.I = I;
+    a.E = E;
+    a.k = k;
+    a.num_sms = sms;
+    a.act = static_cast<int>(act);
+    {
+      StageScope sc(s, MOE_STAGE_DISPATCH);
+      if ((e = launch_fp4_quant_x(a, s)) != cudaSuccess) return cuda_fail(e, "fp4_quant_x");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM1);
+      if ((e = launch_fp4_gate_up(a, s)) != cudaSuccess) return cuda_fail(e, "fp4_gate_up");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM2);
+      if ((e = launch_fp4_down(a, s)) != cudaSuccess) return cuda_fail(e, "fp4_down");
+    }
+    return MOE_OK;
+  }
   if (!fp8 && n <= moe_get_decode_rows()) {
     // small-token path: stream the touched experts' weights once
     DecodeArgs a;
@@ -579,6 +629,21 @@ moe_status moe_quantize_fp8_blocks(const void* wsrc, int nmat, int rows, int col
   cudaError_t e = launch_quantize_blocks(wsrc, nmat, rows, cols, sfmt == MOE_SCALE_UE8M0, q, scale,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "moe_quantize_fp8_blocks launch");
+  return MOE_OK;
+}
+
+moe_status moe_quantize_fp4_blocks(const void* wsrc, int nmat, int rows, int cols, uint8_t* q,
+                                   uint8_t* scale, void* stream) {
+  if (nmat < 0 || rows < 0 || cols < 0)
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp4_blocks: negative size");
+  if (cols % 32) return fail(MOE_ERR_UNSUPPORTED, "moe_quantize_fp4_blocks: cols must be a multiple of 32");
+  if (static_cast<long>(nmat) * rows * cols == 0) return MOE_OK;
+  if (!wsrc || !q || !scale) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp4_blocks: null pointer");
+  if (!aligned(wsrc, 16) || !aligned(q, 16))
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_fp4_blocks: misaligned pointer");
+  cudaError_t e = launch_quantize_fp4(wsrc, static_cast<long>(nmat) * rows, cols, q, scale, num_sms(),
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_quantize_fp4_blocks launch");
   return MOE_OK;
 }
 

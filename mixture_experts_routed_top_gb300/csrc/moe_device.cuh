@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "moe_internal.h"
@@ -253,6 +254,39 @@ __device__ __forceinline__ float gate_act(float g, int act) {
   if (act == MOE_ACT_SILU) return silu_f(g);
   if (act == MOE_ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f));
   return fmaxf(g, 0.0f);
+}
+
+// Smallest power of two >= q (q > 0, fp32), read from q's bits (exact, no
+// log2); *stored gets the biased exponent byte b of the UE8M0 form, scale
+// 2^(b-127).  b is capped at 254 (255 is not a scale).
+__device__ __forceinline__ float ue8m0_ceil(float q, uint32_t* stored) {
+  const uint32_t bits = __float_as_uint(q);
+  int b = static_cast<int>((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+  b = b > 254 ? 254 : b;
+  *stored = static_cast<uint32_t>(b);
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(b) << 23);
+}
+
+// e4m3 scale of one block from its absolute maximum: amax/448 (IEEE fp32
+// division) or the smallest power of two >= that quotient; amax = 0 -> 1.
+// Returns the scale value and its stored form (fp32 bits or exponent byte).
+__device__ __forceinline__ float block_scale(float amax, bool ue8m0, uint32_t* stored) {
+  if (amax == 0.f) {
+    *stored = ue8m0 ? 127u : __float_as_uint(1.0f);
+    return 1.0f;
+  }
+  const float q = amax / 448.0f;
+  if (!ue8m0) {
+    *stored = __float_as_uint(q);
+    return q;
+  }
+  return ue8m0_ceil(q, stored);
+}
+
+// Two fp32 values -> e4m3 codes (round to nearest even, saturating), lo in
+// the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

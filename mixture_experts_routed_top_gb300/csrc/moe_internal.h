@@ -185,4 +185,29 @@ cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk
 cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_idx, int* err,
                                      cudaStream_t s);
 
+// FP4 (e2m1, 1x32 UE8M0 blocks) experts, small-token path only:
+// T*k <= kFusedDecodeRows.  Three kernels: activation quantisation, gate/up
+// with the h quantisation, down with the combine.
+struct Fp4DecodeArgs {
+  const void* hidden;          // bf16 [T, H]
+  const void* w_gate_up;       // packed e2m1 [E, 2I, H/2]
+  const void* w_down;          // packed e2m1 [E, H, I/2]
+  const void* scale_gate_up;   // UE8M0 [E, 2I, H/32]
+  const void* scale_down;      // UE8M0 [E, H, I/32]
+  const int32_t* topk_idx;     // [T, k]
+  const float* topk_w;         // [T, k]
+  float* xdq;                  // fp32 [T, H], quantised activations (scratch)
+  float* hq;                   // fp32 [T*k, I], quantised h (scratch)
+  void* out;                   // bf16 [T, H]
+  int* err;                    // device error word
+  int T, H, I, E, k, num_sms;
+  int act;                     // moe_activation
+};
+cudaError_t launch_fp4_quant_x(const Fp4DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_fp4_gate_up(const Fp4DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_fp4_down(const Fp4DecodeArgs& a, cudaStream_t s);
+// bf16 [rows, cols] -> packed e2m1 [rows, cols/2] + UE8M0 bytes [rows, cols/32]
+cudaError_t launch_quantize_fp4(const void* w, long rows, int cols, uint8_t* q, uint8_t* scale,
+                                int num_sms, cudaStream_t s);
+
 }  // namespace moe

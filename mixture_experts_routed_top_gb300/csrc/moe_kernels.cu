@@ -252,30 +252,6 @@ cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sort
 }
 
 // ============================================================== FP8 helpers
-// Scale of one block from its absolute maximum: amax/448 (IEEE fp32
-// division) or the smallest power of two >= that quotient; amax = 0 -> 1.
-// Returns the scale value and its stored form (fp32 bits or exponent byte).
-__device__ __forceinline__ float block_scale(float amax, bool ue8m0, uint32_t* stored) {
-  if (amax == 0.f) {
-    *stored = ue8m0 ? 127u : __float_as_uint(1.0f);
-    return 1.0f;
-  }
-  const float q = amax / 448.0f;
-  if (!ue8m0) {
-    *stored = __float_as_uint(q);
-    return q;
-  }
-  const uint32_t bits = __float_as_uint(q);
-  int b = static_cast<int>((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
-  b = b > 254 ? 254 : b;
-  *stored = static_cast<uint32_t>(b);
-  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(b) << 23);
-}
-
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));

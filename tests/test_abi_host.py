@@ -27,7 +27,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("moe_route", "moe_dispatch", "moe_experts_forward", "moe_workspace_size",
-              "moe_quantize_fp8_blocks", "moe_last_error"):
+              "moe_quantize_fp8_blocks", "moe_quantize_fp4_blocks", "moe_last_error"):
         assert n in names
 
 
@@ -74,6 +74,29 @@ def test_argument_errors_without_device(L):
         assert fa(p, 4, 128, p, p, 8, 2, 128, p, p, 0, nul, nul, 0, act, p, p, 16, nul) == 5
     assert L.moe_quantize_fp8_blocks(nul, 1, 100, 128, 1, nul, nul, nul) == 2
     assert L.moe_quantize_fp8_blocks(nul, 1, 128, 128, 0, nul, nul, nul) == 1
+
+
+def test_fp4_argument_errors_without_device(L):
+    nul = ctypes.c_void_p(0)
+    p = ctypes.c_void_p(1 << 20)
+    f = L.moe_experts_forward
+    # FP4 weights (wdtype 2) take UE8M0 scales only
+    for sf in (0, 1):
+        assert f(p, 4, 128, p, p, 8, 2, 128, p, p, 2, p, p, sf, p, p, 1 << 30, nul) == 1
+    assert b"UE8M0" in L.moe_last_error()
+    # ... and need both scale buffers
+    assert f(p, 4, 128, p, p, 8, 2, 128, p, p, 2, nul, p, 2, p, p, 1 << 30, nul) == 1
+    # only the small-token path exists for FP4: T*k <= 64
+    assert f(p, 33, 128, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 1 << 30, nul) == 2
+    assert b"T*k" in L.moe_last_error()
+    # T*k = 64 passes those checks and stops at the workspace size
+    assert f(p, 32, 128, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 16, nul) == 5
+    need = L.moe_workspace_size(32, 128, 128, 8, 2, 2)
+    # quantised activations [T, H] and h [T*k, I] are kept in fp32
+    assert need >= 32 * 128 * 4 + 64 * 128 * 4
+    assert L.moe_quantize_fp4_blocks(nul, 1, 4, 48, nul, nul, nul) == 2    # cols % 32
+    assert L.moe_quantize_fp4_blocks(nul, 1, 4, 64, nul, nul, nul) == 1    # null pointers
+    assert L.moe_quantize_fp4_blocks(nul, 0, 4, 64, nul, nul, nul) == 0    # empty
 
 
 def test_decode_rows_setting(L):

@@ -55,3 +55,22 @@ def test_traffic_lookup_follows_the_kernel_source():
         # either the kernel source still hashes as captured, or the entry is ignored
         assert got in (None, ent["bytes_per_launch"])
         assert ent["bytes_per_launch"] == ent["read"] + ent["write"]
+
+
+def test_algorithmic_fp4_weight_bytes_are_half_bytes_plus_block_scales():
+    w = _w("qwen", 1, "fp4", "ue8m0")
+    s = w["shape"]
+    counts = np.zeros(s.E, np.int64)
+    counts[[3, 9, 17, 40]] = 1
+    flops, wbytes, _, touched = bench.algorithmic(w, counts)
+    assert touched == 4
+    assert flops == 6.0 * s.H * s.I * 4
+    # 4 bits per weight and one UE8M0 byte per 32 weights
+    assert wbytes == 4 * (3 * s.H * s.I / 2 + 3 * s.H * s.I / 32)
+
+
+def test_fp4_workloads_stay_on_the_small_token_path():
+    for name, (sname, T, wfmt, sfmt) in bench.WORKLOADS.items():
+        if wfmt == "fp4":
+            s = shape_for(sname, T)
+            assert s.T * s.k <= 64 and sfmt == "ue8m0", name
