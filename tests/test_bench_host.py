@@ -74,3 +74,31 @@ def test_fp4_workloads_stay_on_the_small_token_path():
         if wfmt == "fp4":
             s = shape_for(sname, T)
             assert s.T * s.k <= 64 and sfmt == "ue8m0", name
+
+
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp4"])
+def test_oracle_sample_runs_on_every_weight_format(wfmt):
+    """The CPU legs of bench.py (cpu_baseline and the reference arm) on a
+    tiny workload held in host memory, with the quantised weights made by
+    the oracle's quantisers: the sample selects tokens, copies their experts
+    and runs the matching oracle forward."""
+    import torch
+    import oracle as O
+    from workloads import MoEShape, make_inputs
+    s = MoEShape(T=8, H=256, I=128, E=4, k=2)
+    d = make_inputs(s, seed=0, device="cpu")
+    w = {"shape": s, "wfmt": wfmt, "sfmt": {"bf16": None, "fp8": "f32", "fp4": "ue8m0"}[wfmt],
+         "logits": d["logits"], "hidden": d["hidden"], "w_gate_up": d["w_gate_up"],
+         "w_down": d["w_down"]}
+    if wfmt == "fp8":
+        q, sc, _ = O.quantize_blocks(d["w_gate_up"].float().numpy(), 128, 128, "f32")
+        qd, sd, _ = O.quantize_blocks(d["w_down"].float().numpy(), 128, 128, "f32")
+    elif wfmt == "fp4":
+        q, sc, _ = O.quantize_fp4_blocks(d["w_gate_up"].float().numpy())
+        qd, sd, _ = O.quantize_fp4_blocks(d["w_down"].float().numpy())
+    if wfmt != "bf16":
+        w.update(q_gate_up=torch.from_numpy(q), s_gate_up=torch.from_numpy(sc),
+                 q_down=torch.from_numpy(qd), s_down=torch.from_numpy(sd))
+    smp = bench.OracleSample(w, 4)
+    assert smp.n == 4
+    assert smp.run() > 0.0
