@@ -150,6 +150,8 @@ def dispatch(topk_idx: torch.Tensor, E: int, stream=None):
 
 # ------------------------------------------------------------------ forward
 def workspace_size(T: int, H: int, I: int, E: int, k: int, wdtype: int = W_BF16) -> int:
+    """Bytes of workspace experts_forward needs for these sizes and weight
+    type (W_BF16, W_FP8_E4M3 or W_FP4_E2M1)."""
     return int(lib().moe_workspace_size(T, H, I, E, k, wdtype))
 
 
