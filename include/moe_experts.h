@@ -3,9 +3,9 @@
  * experts forward.
  *
  * What is computed (Hugging Face Transformers "Experts backends" page,
- * introduction): for each token a router selects k experts; the token's
- * hidden state goes through each selected expert's gated MLP (fused gate/up
- * projection, SwiGLU, down projection; backends table, deepgemm_megamoe row,
+ * introduction): every token is sent to the k experts its router ranks
+ * highest; its hidden state goes through each of those experts' gated MLP
+ * (fused gate/up projection, SwiGLU, down projection; backends table, deepgemm_megamoe row,
  * and the SonicMoE section's silu -> SwiGLU mapping) and the k results are
  * summed with the routing weights.  Tokens are ordered by selected expert
  * before the expert GEMMs (backends table, grouped_mm and deepgemm rows).  FP8
@@ -26,8 +26,8 @@
  *   - On a non-OK status nothing was launched (argument errors) or a CUDA
  *     launch failed (MOE_ERR_CUDA); moe_last_error() gives a message.
  *   - Errors are loud: an unsupported shape or format is rejected, never
- *     computed approximately (the page's note on Blackwell scale formats:
- *     fail "instead of silently corrupting the output").
+ *     computed approximately (the page's note on Blackwell scale formats
+ *     prefers a clear error to a wrong result).
  */
 #ifndef MOE_EXPERTS_H
 #define MOE_EXPERTS_H
@@ -62,7 +62,8 @@ int moe_version(void);
 const char* moe_last_error(void);
 
 /*
- * moe_route - router top-k ("a router selects k experts", introduction).
+ * moe_route - router top-k (introduction of the page: per token the router
+ * picks k experts).
  *   logits   device fp32 [T, E]
  *   topk_idx device int32 [T, k]  out: selected experts, slot j ordered by
  *            descending logit, equal logits by ascending expert index
@@ -99,8 +100,9 @@ moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k,
 size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
 
 /*
- * moe_experts_forward - routed experts forward (introduction; gated MLP of
- * the deepgemm_megamoe row; combine "with routing weights").
+ * moe_experts_forward - routed experts forward (introduction: expert
+ * outputs weighted by the routing weights and summed; gated MLP of the
+ * deepgemm_megamoe row).
  *   hidden      device bf16 [T, H]
  *   topk_idx    device int32 [T, k], values in [0, E)
  *   topk_w      device fp32 [T, k]

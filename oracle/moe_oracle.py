@@ -5,9 +5,10 @@ benchmark's CPU-baseline leg may import this module; the product path never
 calls it and shares no code with it.
 
 Source of the method: Hugging Face Transformers documentation page
-"Experts backends" (experts_interface), introduction: for each token a router
-selects k experts, the token's hidden state is projected through the selected
-experts' parameters and the results are aggregated with the routing weights.
+"Experts backends" (experts_interface), introduction: a router ranks the
+experts of every token and keeps k of them; the token's hidden state passes
+through each kept expert, and the k expert outputs are summed with the
+routing weights as coefficients.
 The "eager" row of the backends table describes the plain form this oracle
 follows: loop over the selected experts and apply the projections to their
 tokens.  The gated MLP is "up projection, SwiGLU, down projection" (the
@@ -53,7 +54,7 @@ __all__ = [
     "ACTIVATIONS",
     "expert_mlp", "forward", "forward_brute", "round_to_bf16",
     "bf16_bits_to_f32", "e4m3_encode", "e4m3_decode", "ue8m0_from_quotient",
-    "quantize_blocks", "dequantize_blocks", "forward_fp8",
+    "quantize_blocks", "dequantize_blocks", "requantize_rows", "forward_fp8",
     "e2m1_encode", "e2m1_decode", "pack_e2m1", "unpack_e2m1", "quantize_fp4_blocks",
     "dequantize_fp4_blocks", "forward_fp4",
     "touched_weight_bytes", "rel_max_err",
@@ -86,7 +87,7 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# Router ("For each token, a router selects k experts", introduction)
+# Router (introduction of the page: a router picks the top-k experts of each token)
 # --------------------------------------------------------------------------
 
 def route(logits: np.ndarray, k: int):
@@ -127,7 +128,8 @@ def route_weights_full_softmax(logits: np.ndarray, idx: np.ndarray) -> np.ndarra
 
 
 # --------------------------------------------------------------------------
-# Dispatch ("orders tokens by selected experts", grouped_mm / deepgemm rows)
+# Dispatch (grouped_mm / deepgemm rows of the backends table: tokens are sorted
+# by their selected expert before one grouped GEMM)
 # --------------------------------------------------------------------------
 
 def dispatch(topk_idx: np.ndarray, E: int):
@@ -396,6 +398,16 @@ def scale_values(stored: np.ndarray, fmt: str) -> np.ndarray:
     return np.ldexp(np.float32(1.0), b - 127).astype(np.float32)
 
 
+def requantize_rows(x: np.ndarray, block: int, fmt: str) -> np.ndarray:
+    """Dynamic activation quantisation ("FP8 and FP4 quantized experts"
+    section: activation scales are computed on the fly, per row): each row of
+    x [M, C] (taken as fp32) is cut into 1 x block blocks along C, quantised
+    to e4m3 codes with the block's scale in ``fmt`` and returned as the
+    dequantised values (float64)."""
+    q, _, s = quantize_blocks(np.asarray(x, dtype=np.float32), 1, block, fmt)
+    return dequantize_blocks(q, s, 1, block)
+
+
 def forward_fp8(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down,
                 ws_down, fmt: str, quantize_act: bool = True,
                 quantize_h: bool = True, act: str = "silu") -> np.ndarray:
@@ -419,16 +431,12 @@ def forward_fp8(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down,
         toks = rows // k
         slots = rows % k
         x = np.asarray(hidden[toks], dtype=np.float32)
-        if quantize_act:
-            xq, _, xs = quantize_blocks(x, 1, 128, fmt)
-            x = dequantize_blocks(xq, xs, 1, 128)
-        x = np.asarray(x, dtype=np.float64)
+        x = requantize_rows(x, 128, fmt) if quantize_act else x.astype(np.float64)
         g = x @ wgu[e, :I].T
         u = x @ wgu[e, I:].T
         h = ACTIVATIONS[act](g) * u
         if quantize_h:
-            hq, _, hs = quantize_blocks(h.astype(np.float32), 1, 128, fmt)
-            h = dequantize_blocks(hq, hs, 1, 128)
+            h = requantize_rows(h, 128, fmt)
         y = h @ wd[e].T
         np.add.at(out, toks, w[toks, slots][:, None] * y)
     return out
@@ -520,12 +528,6 @@ def dequantize_fp4_blocks(packed: np.ndarray, scales: np.ndarray, block: int = 3
     return v * np.repeat(np.asarray(scales, dtype=dtype), block, axis=-1)
 
 
-def _e4m3_rows_1xb(x: np.ndarray, block: int) -> np.ndarray:
-    """Dynamic e4m3 quantisation of rows in 1 x block UE8M0 blocks, dequantised."""
-    q, _, s = quantize_blocks(np.asarray(x, dtype=np.float32), 1, block, "ue8m0")
-    return dequantize_blocks(q, s, 1, block)
-
-
 def forward_fp4(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down, ws_down,
                 block: int = 32, quantize_act: bool = True, quantize_h: bool = True,
                 act: str = "silu") -> np.ndarray:
@@ -549,12 +551,12 @@ def forward_fp4(hidden, topk_idx, topk_w, wq_gate_up, ws_gate_up, wq_down, ws_do
         toks = rows // k
         slots = rows % k
         x = np.asarray(hidden[toks], dtype=np.float32)
-        x = _e4m3_rows_1xb(x, block) if quantize_act else x.astype(np.float64)
+        x = requantize_rows(x, block, "ue8m0") if quantize_act else x.astype(np.float64)
         g = x @ wgu[e, :I].T
         u = x @ wgu[e, I:].T
         h = ACTIVATIONS[act](g) * u
         if quantize_h:
-            h = _e4m3_rows_1xb(h, block)
+            h = requantize_rows(h, block, "ue8m0")
         y = h @ wd[e].T
         np.add.at(out, toks, w[toks, slots][:, None] * y)
     return out
