@@ -8,8 +8,9 @@ and inputs are resident in HBM when the timed region starts (``value``);
 ``e2e`` repeats the measurement through host buffers with the copies inside
 the timed region.
 
-Default workload: the Qwen1.5-MoE-A2.7B-shaped layer in prefill (T=4096,
-H=2048, I=1408, E=60, k=4), bf16.  ``--workload`` selects another one.
+Default workload: the DeepSeek-V3-shaped layer in prefill (T=8192, H=7168,
+I=2048, E=256, k=8, Zipf(1.1) expert skew), bf16, the largest of the
+single-GPU workloads.  ``--workload`` selects another one.
 
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); ``value`` is the tokens of all ranks divided by
@@ -460,6 +461,7 @@ def run_ours(args, rank, world, local_rank):
     e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
+    e2e_outs = {"serial": o_host.clone()}
 
     # The same, overlapped as a serving loop would run it: step i+1's inputs
     # go host -> device on one copy stream and step i-1's output device ->
@@ -521,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
         ge.record(stream)
         torch.cuda.synchronize()
         e2e_graph_ms = max_over_ranks(gs.elapsed_time(ge), dev)
+        e2e_outs["graph"] = o_host.clone()
 
     overlapped(max(2, args.warmup // 2))
     torch.cuda.synchronize()
@@ -533,12 +536,14 @@ def run_ours(args, rank, world, local_rank):
     o_end.record(stream)
     torch.cuda.synchronize()
     e2e_ov_ms = max_over_ranks(o_start.elapsed_time(o_end), dev)
-    # both end-to-end outputs agree with the device-resident run: the fp32
-    # combine's order may move a bf16 rounding by one unit at the largest
-    # outputs (~2 % of rms), far below what a torn or stale buffer gives
+    # every end-to-end loop's output agrees with the device-resident run: the
+    # fp32 combine's order may move a bf16 rounding by one unit at the
+    # largest outputs (~2 % of rms), far below what a torn or stale buffer
+    # gives
     ref_out = out.float().cpu()
     rms = ref_out.pow(2).mean().sqrt().item() or 1.0
-    for name, got in (("serial", o_host), ("overlapped", oh[(args.steps - 1) & 1])):
+    e2e_outs["overlapped"] = oh[(args.steps - 1) & 1]
+    for name, got in e2e_outs.items():
         dev_max = (got.float() - ref_out).abs().max().item()
         if dev_max > 5e-2 * rms:
             raise RuntimeError(f"{name} end-to-end output differs from the device-resident run "
@@ -648,7 +653,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen-prefill", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="dsv3-prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

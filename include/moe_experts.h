@@ -276,9 +276,12 @@ int moe_profile_read(float* stage_ms, int* stage_launches, int n);
  * loads the library until the process exits) and allocates nothing.  The
  * caller still passes the inputs and the four outputs, with the same meaning
  * and layout as moe_dispatch.
- *   - Sizes whose moe_dispatch_workspace_size(T, E, k) exceeds the fixed
- *     scratch are rejected with MOE_ERR_UNSUPPORTED before anything is
- *     launched; moe_dispatch with a caller workspace has no such limit.
+ *   - E, k and T*k have the same limits as moe_dispatch (E <= 1024,
+ *     k <= min(E, 32), T*k < 2^31) and are checked first.  Every size those
+ *     limits accept needs at most about 535 KB of scratch, so the fixed
+ *     array always suffices; its size check (MOE_ERR_UNSUPPORTED when
+ *     moe_dispatch_workspace_size(T, E, k) exceeds it, before anything is
+ *     launched) is only a guard.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

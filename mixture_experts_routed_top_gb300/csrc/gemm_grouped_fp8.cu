@@ -28,6 +28,8 @@
 // All waits are bounded as in the bf16 kernel.
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -456,11 +458,13 @@ cudaError_t launch_fp8_impl(const GroupedGemmFp8Args& a, cudaStream_t s) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  static bool attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev]) {
+  // one flag per device; any host thread may launch, so the flags are atomic
+  // (setting the attribute twice is harmless, reading a torn flag is not)
+  static std::atomic<bool> attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L8::SMEM);
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   Fp8Dev p;
   p.offsets = a.offsets;

@@ -26,6 +26,8 @@
 // +128), warps 2-5 epilogue (tcgen05.ld 32x32b, thread = feature).  Tiles
 // run in (expert, feature block, token tile) order.  Every mbarrier wait is
 // bounded.
+#include <atomic>
+
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -319,11 +321,13 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  static bool attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev]) {
+  // one flag per device; any host thread may launch, so the flags are atomic
+  // (setting the attribute twice is harmless, reading a torn flag is not)
+  static std::atomic<bool> attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   GemmDev p;
   p.offsets = a.offsets;

@@ -33,6 +33,18 @@ constexpr size_t kNoAllocScratchBytes = MOE_DISPATCH_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kNoAllocScratchBytes];
 
+// Largest dispatch scratch any accepted size needs: the error-word block,
+// the m-tile prefix and the touched list (E+1 ints each), and the per-chunk
+// expert counts (at most 128 chunks of E ints), each region 1024-byte
+// aligned.  The fixed array covers it, so the size check below is only a
+// guard against a future change of that layout.
+constexpr size_t align1k(size_t x) { return (x + 1023) / 1024 * 1024; }
+constexpr size_t kMaxDispatchScratch = align1k(sizeof(moe::WsHeader)) +
+                                       2 * align1k((moe::kMaxE + 1) * 4) +
+                                       align1k(128 * static_cast<size_t>(moe::kMaxE) * 4);
+static_assert(kMaxDispatchScratch <= kNoAllocScratchBytes,
+              "the fixed dispatch scratch must hold every accepted size");
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
@@ -64,6 +76,14 @@ moe_status moe_dispatch_noalloc(const int32_t* topk_idx, int T, int E, int k, in
                                 void* stream) {
   if (T < 0 || E < 1 || k < 1)
     return moe::set_last_error(MOE_ERR_INVALID_ARG, "moe_dispatch_noalloc: bad sizes");
+  if (E > moe::kMaxE)
+    return moe::set_last_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_noalloc: E must be in [1, %d]",
+                               moe::kMaxE);
+  if (k > E || k > moe::kMaxK)
+    return moe::set_last_error(MOE_ERR_UNSUPPORTED,
+                               "moe_dispatch_noalloc: k must be in [1, min(E, %d)]", moe::kMaxK);
+  if (static_cast<long>(T) * k > 0x7FFFFFFFL)
+    return moe::set_last_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_noalloc: T*k exceeds int32");
   const size_t need = moe_dispatch_workspace_size(T, E, k);
   if (need > kNoAllocScratchBytes)
     return moe::set_last_error(MOE_ERR_UNSUPPORTED,

@@ -136,9 +136,15 @@ def test_forward_fp8_rejects_missing_scales(moe):
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("T,fmt,ntok", [(64, "f32", 64), (64, "ue8m0", 64),
-                                        (16384, "f32", 4), (16384, "ue8m0", 4)])
-def test_forward_fp8_full_size_sampled(moe, T, fmt, ntok):
+@pytest.mark.parametrize("T,fmt", [(64, "f32"), (64, "ue8m0"), (16384, "f32"), (16384, "ue8m0")])
+def test_forward_fp8_full_size_every_tile(moe, T, fmt):
+    """Full FP8 workload size on the GPU.  At T = 64 every token is checked.
+    At T = 16384 the oracle recomputes the tokens at the edges of every
+    grouped-GEMM tile of the busiest expert (125 tiles of 128 rows) and the
+    first and last token of the other popular experts, using only tokens
+    whose eight experts are all among the 16 most popular (more if some tile
+    has no such token), so that few experts are dequantised on the host."""
+    from full_size_sampling import fp8_expert_fn, oracle_on_tokens, probe_tokens
     shape = shape_for("dsv3_fp8", T)
     d = make_inputs(shape, seed=0, device="cuda")
     qgu, sgu = moe.quantize_fp8_blocks(d["w_gate_up"], fmt)
@@ -148,18 +154,21 @@ def test_forward_fp8_full_size_sampled(moe, T, fmt, ntok):
     out = moe.experts_forward(d["hidden"], idx, w, qgu, qd, scale_gate_up=sgu, scale_down=sd,
                               scale_fmt=fmt)
     moe.workspace_status(moe.default_workspace())
-    ref_idx, _ = O.route(d["logits"].cpu().numpy(), shape.k)
+    ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
-    toks = np.sort(np.random.default_rng(1).choice(T, ntok, replace=False))
-    sub = ref_idx[toks]
-    experts = np.unique(sub)
-    remap = np.full(shape.E, -1, np.int64)
-    remap[experts] = np.arange(len(experts))
-    et = torch.from_numpy(experts).long().cuda()
-    ref = O.forward_fp8(d["hidden"][torch.from_numpy(toks).cuda()].float().cpu().numpy(),
-                        remap[sub].astype(np.int32), w.cpu().numpy()[toks],
-                        qgu.index_select(0, et).cpu().numpy(), sgu.index_select(0, et).cpu().numpy(),
-                        qd.index_select(0, et).cpu().numpy(), sd.index_select(0, et).cpu().numpy(),
-                        fmt)
-    got = out[torch.from_numpy(toks).cuda()].float().cpu().numpy()
+    if T <= 64:
+        toks = np.arange(T)
+    else:
+        counts = np.bincount(ref_idx.ravel(), minlength=shape.E)
+        order = np.argsort(-counts, kind="stable")
+        for n_cheap in (16, 24, 32, 48):          # widen until every hot tile is reached
+            cheap = set(order[:n_cheap].tolist())
+            toks, counts, hot, reached = probe_tokens(ref_idx, shape.E, shape.k, cheap=cheap)
+            if reached == 2 * -(-int(counts[hot]) // 128):
+                break
+        assert hot in cheap and reached == 2 * -(-int(counts[hot]) // 128)
+    tt = torch.from_numpy(toks).cuda()
+    ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
+                           fp8_expert_fn(qgu, sgu, qd, sd, fmt))
+    got = out[tt].float().cpu().numpy()
     assert O.rel_max_err(got, ref) <= FP8_TOL

@@ -293,10 +293,13 @@ def test_forward_bf16_repeatable_and_token_order_equivariant(moe):
     assert (b - ref).abs().max().item() <= 1e-2 * ref.pow(2).mean().sqrt().item()
 
 
-@pytest.mark.parametrize("name,T,ntok", [("qwen", 4096, 48), ("dsv3", 8192, 4)])
-def test_forward_bf16_full_size_sampled(moe, name, T, ntok):
-    """Full workload size on the GPU; the oracle recomputes a sample of tokens
-    (each token's output depends only on its own row and its experts)."""
+@pytest.mark.parametrize("name,T", [("qwen", 4096), ("dsv3", 8192)])
+def test_forward_bf16_full_size_every_tile(moe, name, T):
+    """Full workload size on the GPU, through the default path choice; the
+    oracle recomputes the tokens at the edges of every grouped-GEMM tile of
+    the busiest expert (63 tiles of 128 rows for the skewed DeepSeek-V3
+    layer) and the first and last token of every other touched expert."""
+    from full_size_sampling import bf16_expert_fn, oracle_on_tokens, probe_tokens
     shape = shape_for(name, T)
     d = make_inputs(shape, seed=0, device="cuda")
     idx, w = moe.route(d["logits"], shape.k)
@@ -304,20 +307,84 @@ def test_forward_bf16_full_size_sampled(moe, name, T, ntok):
     moe.workspace_status(moe.default_workspace())
     ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
-    rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(T, ntok, replace=False))
-    sub_idx = ref_idx[toks]
-    experts = np.unique(sub_idx)
-    # oracle on the sampled tokens with only their experts, renumbered
-    remap = {int(e): i for i, e in enumerate(experts)}
-    loc_idx = np.vectorize(remap.get)(sub_idx).astype(np.int32)
-    ex_t = torch.from_numpy(experts).long().cuda()
-    wgu = d["w_gate_up"].index_select(0, ex_t).float().cpu().numpy()
-    wd = d["w_down"].index_select(0, ex_t).float().cpu().numpy()
-    hid = d["hidden"][torch.from_numpy(toks).cuda()].float().cpu().numpy()
-    ref = O.forward(hid, loc_idx, w.cpu().numpy()[toks], wgu, wd, dtype=np.float32)
-    got = out[torch.from_numpy(toks).cuda()].float().cpu().numpy()
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+    toks, counts, hot, reached = probe_tokens(ref_idx, shape.E, shape.k)
+    n_tiles = 2 * -(-int(counts[hot]) // 128)
+    assert reached == n_tiles
+    tt = torch.from_numpy(toks).cuda()
+    ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
+                           bf16_expert_fn(d["w_gate_up"], d["w_down"]))
+    got = out[tt].float().cpu().numpy()
     assert O.rel_max_err(got, ref) <= BF16_TOL
+
+
+def _replay_case(moe, shape, seeds, fp8=None):
+    """Router + experts_forward captured once as a CUDA graph on fixed device
+    buffers; every replay follows a copy of new logits and hidden rows into
+    those buffers.  Yields (out after the replay, oracle output)."""
+    base = make_inputs(shape, seed=seeds[0], device="cpu")
+    wgu, wd = base["w_gate_up"].cuda(), base["w_down"].cuda()
+    kw = dict(w_gate_up=wgu, w_down=wd)
+    if fp8 is not None:
+        qgu, sgu = moe.quantize_fp8_blocks(wgu, fp8)
+        qd, sd = moe.quantize_fp8_blocks(wd, fp8)
+        kw = dict(w_gate_up=qgu, w_down=qd, scale_gate_up=sgu, scale_down=sd, scale_fmt=fp8)
+    logits = base["logits"].cuda()
+    hidden = base["hidden"].cuda()
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device="cuda")
+    ws = moe.Workspace("cuda")
+
+    def step():
+        idx, w = moe.route(logits, shape.k)
+        moe.experts_forward(hidden, idx, w, out=out, workspace=ws, **kw)
+
+    step()                                       # lazy set-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in seeds[1:]:
+        d = make_inputs(shape, seed=seed, device="cpu")
+        logits.copy_(d["logits"].cuda())
+        hidden.copy_(d["hidden"].cuda())
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        moe.workspace_status(ws)
+        ref_idx, ref_w = O.route(d["logits"].numpy(), shape.k)
+        hid = d["hidden"].float().numpy()
+        if fp8 is None:
+            ref = O.forward(hid, ref_idx, ref_w, base["w_gate_up"].float().numpy(),
+                            base["w_down"].float().numpy())
+        else:
+            ref = O.forward_fp8(hid, ref_idx, ref_w, qgu.cpu().numpy(), sgu.cpu().numpy(),
+                                qd.cpu().numpy(), sd.cpu().numpy(), fp8)
+        yield out.float().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("path,shape", [
+    ("rows", MoEShape(T=300, H=256, I=384, E=6, k=3)),
+    ("swap", MoEShape(T=300, H=256, I=384, E=6, k=3)),
+    ("decode", MoEShape(T=4, H=512, I=256, E=16, k=4)),      # the two fused decode kernels
+    ("decode", MoEShape(T=40, H=512, I=256, E=16, k=4)),     # dispatch, two GEMVs, combine
+], indirect=["path"])
+def test_graph_replay_matches_oracle(moe, shape, path):
+    """What the benchmark times: the whole step as a replayed CUDA graph,
+    every kernel chained by programmatic dependent launch.  Each replay's
+    output (after new inputs were copied into the captured buffers) must
+    match the oracle on those inputs."""
+    n = 0
+    for got, ref in _replay_case(moe, shape, seeds=(20, 21, 22)):
+        assert O.rel_max_err(got, ref) <= BF16_TOL
+        n += 1
+    assert n == 2
+
+
+@pytest.mark.parametrize("fmt", ["f32", "ue8m0"])
+def test_graph_replay_matches_oracle_fp8(moe, fmt):
+    shape = MoEShape(T=300, H=512, I=384, E=6, k=3)
+    for got, ref in _replay_case(moe, shape, seeds=(30, 31, 32), fp8=fmt):
+        assert O.rel_max_err(got, ref) <= 6e-2
 
 
 # ----------------------------------------------------------------- error paths

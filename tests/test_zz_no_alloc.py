@@ -45,14 +45,19 @@ def test_dispatch_noalloc_matches_workspace_dispatch_two_calls():
             assert torch.equal(got, want)
 
 
-def test_dispatch_noalloc_rejects_sizes_beyond_its_scratch():
+def test_dispatch_noalloc_rejects_out_of_range_sizes_before_any_launch():
+    """E and k outside moe_dispatch's limits are rejected up front (every
+    size inside them fits the fixed scratch, so the scratch-size guard is
+    never what rejects a call)."""
     import mixture_experts_routed_top_gb300 as moe
     L = moe.lib()
     fn = _entry(L)
     nul = ctypes.c_void_p(0)
     n0 = moe.launch_count()
-    # 128 histogram blocks x 4096 experts x 4 B = 2 MiB of scratch > 1 MiB
     st = fn(nul, 10_000_000, 4096, 8, nul, nul, nul, nul, nul)
     assert st == 2
-    assert b"scratch" in L.moe_last_error()
+    assert b"E must be" in L.moe_last_error()
+    st = fn(nul, 100, 8, 9, nul, nul, nul, nul, nul)
+    assert st == 2
+    assert b"k must be" in L.moe_last_error()
     assert moe.launch_count() == n0
