@@ -53,18 +53,24 @@ WORKLOADS = {
     # profiling-sized layers (32 experts), used for ncu captures
     "dsv3e32-fp8-2048-f32": ("dsv3_e32", 2048, "fp8", "f32"),
     "dsv3e32-fp8-8-f32": ("dsv3_e32", 8, "fp8", "f32"),
-    # FP4 (e2m1, 1x32 UE8M0 blocks) experts: small-token batches only
+    "dsv3e32-fp8-2048-ue8m0": ("dsv3_e32", 2048, "fp8", "ue8m0"),
+    "dsv3e32-fp4-2048": ("dsv3_e32", 2048, "fp4", "ue8m0"),
+    "dsv3e32-prefill": ("dsv3_e32", 2048, "bf16", None),
+    # FP4 (e2m1, 1x32 UE8M0 blocks) experts: GEMVs up to 64 routed rows,
+    # block-scaled tensor-core GEMMs above
     "qwen-fp4-decode-1": ("qwen", 1, "fp4", "ue8m0"),
     "qwen-fp4-decode-16": ("qwen", 16, "fp4", "ue8m0"),
     "dsv3-fp4-1": ("dsv3", 1, "fp4", "ue8m0"),
     "dsv3-fp4-8": ("dsv3", 8, "fp4", "ue8m0"),
+    "qwen-fp4-prefill": ("qwen", 4096, "fp4", "ue8m0"),
+    "dsv3-fp4-prefill": ("dsv3", 8192, "fp4", "ue8m0"),
 }
 DESCRIPTIONS = {
     "qwen": "Qwen1.5-MoE-A2.7B-shaped MoE layer",
     "tiny": "tiny MoE FFN",
     "dsv3": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) expert skew",
     "dsv3_fp8": "DeepSeek-V3-shaped MoE layer, Zipf(1.1) skew, e4m3 128x128 block-scaled weights",
-    "dsv3_e32": "DeepSeek-V3-width MoE layer with 32 experts (profiling size), e4m3 weights",
+    "dsv3_e32": "DeepSeek-V3-width MoE layer with 32 experts (profiling size)",
 }
 L2_BYTES = 129 * 2 ** 20
 BYTES_PER_WEIGHT = {"bf16": 2.0, "fp8": 1.0, "fp4": 0.5}
@@ -73,9 +79,13 @@ DTYPE_NAME = {"bf16": "bf16", "fp8": "fp8-e4m3", "fp4": "fp4-e2m1"}
 
 
 def describe(name):
-    sname, _, wfmt, _ = WORKLOADS[name]
+    sname, _, wfmt, sfmt = WORKLOADS[name]
     d = DESCRIPTIONS[sname]
-    return d + ", packed e2m1 weights with 1x32 UE8M0 scales" if wfmt == "fp4" else d
+    if wfmt == "fp4":
+        return d + ", packed e2m1 weights with 1x32 UE8M0 scales"
+    if wfmt == "fp8" and "e4m3" not in d:
+        return d + f", e4m3 weights with 128x128 {sfmt} scales"
+    return d
 
 
 def log(*a):
@@ -338,6 +348,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     moe.lib(build_if_missing=True)
     moe.set_swap_rows({"auto": -1, "rows": 0, "swap": 1 << 20}[args.bf16_gemm])
+    moe.set_block_scaled_mma(args.ue8m0_kernel == "block-scaled")
+    if args.tile_group is not None:
+        moe.set_tile_group(args.tile_group)
+    if args.decode_kernels is not None:
+        moe.set_decode_single(args.decode_kernels == 1)
     w = build_workload(args.workload, dev)
     w["act"] = args.activation
     s = w["shape"]
@@ -567,14 +582,17 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
     else:
-        pk = peaks["bf16_tflops"] * (2.0 if w["wfmt"] == "fp8" else 1.0)
+        # e4m3 x e4m3 and e4m3 x e2m1 (kind::mxf8f6f4) run at the FP8 rate
+        pk = peaks["bf16_tflops"] * (2.0 if w["wfmt"] in ("fp8", "fp4") else 1.0)
         achieved = kern_flops / d_avg_s / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
                 "unit": "TFLOP/s", "frac": round(achieved / pk, 4)}
     peak_kind = ("hbm_gbs, STREAM-style copy" if hbm_bound else
                  "bf16 burst" if w["wfmt"] == "bf16" else "bf16 burst x2 nominal fp8/bf16 ratio")
+    mx_path = (w["wfmt"] == "fp8" and w["sfmt"] == "ue8m0" and moe.get_block_scaled_mma()) or \
+              (w["wfmt"] == "fp4" and s.T * s.k > moe.get_fp4_gemv_rows())
     # the same kernel against the other roof (both matter near the ridge)
-    if w["wfmt"] == "fp4":
+    if w["wfmt"] == "fp4" and not mx_path:
         # the FP4 GEMVs run their multiply-adds on CUDA cores: fp32 FMA peak
         # = SMs x 128 lanes x 2 flops x the largest SM clock seen
         props = torch.cuda.get_device_properties(dev)
@@ -616,7 +634,14 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("flushed before every timed step (512 MB write)" if flush else
                           f"inputs larger than L2 ({working_set / 1e9:.2f} GB touched per step)"),
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
-                   "bf16_gemm": args.bf16_gemm, "activation": args.activation,
+                   "bf16_gemm": args.bf16_gemm, "tile_group": moe.get_tile_group(),
+                   "decode_kernels": 1 if moe.get_decode_single() else 2,
+                   "activation": args.activation,
+                   "scaled_kernels": ("block-scaled tensor-core MMA (kind::mxf8f6f4, UE8M0)"
+                                      if mx_path else
+                                      "CUDA-core GEMVs" if w["wfmt"] == "fp4" else
+                                      "software promotion of per-K-block partial sums"
+                                      if w["wfmt"] == "fp8" else None),
                    "timed_steps": "CUDA graph replays of one captured step" if args.graph
                                   else "steps launched from Python",
                    "stage_timing": ("per-stage CUDA events in a second capture of the same "
@@ -660,6 +685,14 @@ def main():
                     help="launch every timed step from Python instead of replaying a CUDA graph")
     ap.add_argument("--bf16-gemm", default="auto", choices=["auto", "rows", "swap"],
                     help="orientation of the bf16 grouped GEMMs (library default: auto)")
+    ap.add_argument("--ue8m0-kernel", default="block-scaled", choices=["block-scaled", "promotion"],
+                    help="FP8 experts with UE8M0 scales: tensor-core block scaling (library "
+                         "default) or the software promotion kernel")
+    ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],
+                    help="small bf16 decode batches as one cooperative kernel or two kernels "
+                         "(library default)")
+    ap.add_argument("--tile-group", type=int, default=None,
+                    help="m-tiles per tile group of the token-row gate/up GEMM (library default)")
     ap.add_argument("--activation", default="silu", choices=["silu", "gelu", "relu"],
                     help="gate activation: SwiGLU (default), GeGLU or ReGLU experts")
     args = ap.parse_args()

@@ -100,6 +100,18 @@ moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k,
 size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
 
 /*
+ * moe_workspace_accumulator_offset - byte offset, inside a workspace sized
+ * by moe_workspace_size() with the same arguments, of the fp32 accumulator
+ * [T, H] into which the grouped paths sum the weighted expert outputs before
+ * the single rounding to bf16.  After such a forward (every path except the
+ * small-token GEMVs: bf16 with T*k <= moe_get_decode_rows(), FP4 with
+ * T*k <= moe_get_fp4_gemv_rows()) and until the next call on the workspace,
+ * it holds the un-rounded output, and out is its round-to-nearest-even bf16
+ * image.  Meant for checking results; 0 for invalid sizes.
+ */
+size_t moe_workspace_accumulator_offset(int T, int H, int I, int E, int k, moe_wdtype wdtype);
+
+/*
  * moe_experts_forward - routed experts forward (introduction: expert
  * outputs weighted by the routing weights and summed; gated MLP of the
  * deepgemm_megamoe row).
@@ -123,12 +135,20 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype);
  *               along the contraction axis: scale_gate_up [E, 2I, H/32],
  *               scale_down [E, H, I/32]; sfmt must be MOE_SCALE_UE8M0.  The
  *               hidden rows and the SwiGLU output are quantised on the fly to
- *               e4m3 in 1x32 UE8M0 blocks.  Only the small-token path exists
- *               for this format: T*k <= 64, else MOE_ERR_UNSUPPORTED.
+ *               e4m3 in 1x32 UE8M0 blocks.  Up to 64 routed rows (T*k, see
+ *               moe_set_fp4_gemv_rows) CUDA-core GEMVs stream the packed
+ *               weights; above that block-scaled tensor-core GEMMs run, which
+ *               need H % 256 == 0 (else MOE_ERR_UNSUPPORTED) and 32-byte
+ *               aligned weight buffers (else MOE_ERR_INVALID_ARG).
  *   out         device bf16 [T, H]: out[t] = sum_j topk_w[t,j] *
  *               down(silu(gate x_t) * up x_t) of expert topk_idx[t,j],
  *               accumulated in fp32 and rounded once to bf16
- *   ws          device scratch, >= moe_workspace_size() bytes, 256-B aligned
+ *   ws          device scratch, >= moe_workspace_size() bytes, 256-B aligned;
+ *               its first 256 bytes must be zero before the first forward
+ *               that uses it (they hold the device error word and two
+ *               counters of the small-token decode kernel; the library
+ *               leaves them zero after every call, and moe_workspace_status
+ *               resets them after an error)
  * Requirements: H % 128 == 0 (H % 256 == 0 for FP8 weights), I % 128 == 0,
  * 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 is a no-op).  Other
  * shapes: MOE_ERR_UNSUPPORTED.
@@ -236,6 +256,51 @@ int moe_get_decode_rows(void);
  */
 void moe_set_swap_rows(int rows_per_expert);
 int moe_get_swap_rows(void);
+
+/*
+ * moe_set_tile_group - tile order of the token-row gate/up GEMM.  Inside an
+ * expert the 128-row m-tiles run in groups of m_tiles: every n-tile of one
+ * group (m fastest), then the next group, so that an expert with many rows
+ * re-reads one group's activation tiles per n-tile instead of all of them.
+ * 0 (the default) puts all of an expert's m-tiles in one group.
+ * Process-wide; moe_get_tile_group returns the setting.
+ */
+void moe_set_tile_group(int m_tiles);
+int moe_get_tile_group(void);
+
+/*
+ * moe_set_decode_single - bf16 forwards with at most 64 routed rows on the
+ * small-token path run as one cooperative kernel (on != 0: the gate/up
+ * GEMV, then the down GEMV and combine, whose weight loads start before the
+ * last h values are ready) or as two kernels (on == 0, the default, measured
+ * faster).  If the GPU cannot hold the single kernel's grid at once, the two
+ * kernels run.
+ * Process-wide; moe_get_decode_single returns the setting.
+ */
+void moe_set_decode_single(int on);
+int moe_get_decode_single(void);
+
+/*
+ * moe_set_block_scaled_mma - how UE8M0 block scales of FP8 experts are
+ * applied.  on != 0 (the default): by the tensor core's block scaling
+ * (tcgen05.mma kind::mxf8f6f4, one UE8M0 byte per 32-wide K sub-block of
+ * every row and column), so no software promotion runs; on == 0: by the
+ * software promotion kernel that float32 scales always use.  Both give the
+ * same mathematics (scales are powers of two; only the fp32 summation order
+ * differs).  Process-wide; moe_get_block_scaled_mma returns the setting.
+ */
+void moe_set_block_scaled_mma(int on);
+int moe_get_block_scaled_mma(void);
+
+/*
+ * moe_set_fp4_gemv_rows - FP4 forwards with T*k <= rows run on the
+ * CUDA-core GEMVs (small-token path), larger ones on the block-scaled
+ * tensor-core GEMMs.  rows < 0 restores the default (64, also the maximum);
+ * 0 sends every FP4 forward to the tensor-core GEMMs.  Process-wide;
+ * moe_get_fp4_gemv_rows returns the threshold in use.
+ */
+void moe_set_fp4_gemv_rows(int rows);
+int moe_get_fp4_gemv_rows(void);
 
 /*
  * Stage timing: between moe_profile_begin() and moe_profile_end() every

@@ -20,7 +20,9 @@ __all__ = [
     "MoEError", "lib", "route", "dispatch", "dispatch_workspace_size", "workspace_size",
     "experts_forward", "quantize_fp8_blocks", "quantize_fp4_blocks", "workspace_status", "set_decode_rows",
     "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
-    "selftest_wait_timeout", "launch_count",
+    "selftest_wait_timeout", "launch_count", "accumulator", "set_block_scaled_mma",
+    "get_block_scaled_mma", "set_fp4_gemv_rows", "get_fp4_gemv_rows", "set_decode_single",
+    "get_decode_single", "set_tile_group", "get_tile_group",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "W_FP4_E2M1", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0", "ACTIVATIONS",
 ]
@@ -65,6 +67,15 @@ _SIGS = {
     "moe_profile_read": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _I], _I),
     "moe_selftest_wait_timeout": ([_P, _SZ, _I, _P], _I),
     "moe_launch_count": ([], ctypes.c_longlong),
+    "moe_workspace_accumulator_offset": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_set_block_scaled_mma": ([_I], None),
+    "moe_get_block_scaled_mma": ([], _I),
+    "moe_set_tile_group": ([_I], None),
+    "moe_get_tile_group": ([], _I),
+    "moe_set_decode_single": ([_I], None),
+    "moe_get_decode_single": ([], _I),
+    "moe_set_fp4_gemv_rows": ([_I], None),
+    "moe_get_fp4_gemv_rows": ([], _I),
 }
 
 
@@ -187,8 +198,8 @@ def experts_forward(hidden: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.
     w_gate_up [E,2I,H] and w_down [E,H,I], bf16 or e4m3 bytes (uint8 or
     float8_e4m3fn) with 128x128 block scales (scale_fmt 'f32' or 'ue8m0'),
     or packed e2m1 bytes (uint8 or int8) [E,2I,H/2] and [E,H,I/2] with 1x32
-    UE8M0 scales from quantize_fp4_blocks (T*k <= 64 only); activation: the gate activation, 'silu' (SwiGLU), 'gelu' (GeGLU, exact
-    erf GELU) or 'relu' (ReGLU)."""
+    UE8M0 scales from quantize_fp4_blocks; activation: the gate activation,
+    'silu' (SwiGLU), 'gelu' (GeGLU, exact erf GELU) or 'relu' (ReGLU)."""
     _need_cuda(hidden, topk_idx, topk_w, w_gate_up, w_down, scale_gate_up, scale_down, out)
     T, H = hidden.shape
     k = topk_idx.shape[1]
@@ -231,6 +242,18 @@ def workspace_status(workspace, stream=None):
     """Synchronise and raise MoEError if a kernel flagged an error in ws."""
     ws = workspace.buf if isinstance(workspace, Workspace) else workspace
     _check(lib().moe_workspace_status(_ptr(ws), _stream(stream)))
+
+
+def accumulator(workspace, T: int, H: int, I: int, E: int, k: int,
+                wdtype: int = W_BF16) -> torch.Tensor:
+    """fp32 [T, H] view of the workspace's output accumulator: after a
+    grouped-path forward with these sizes it holds the un-rounded output
+    (see moe_workspace_accumulator_offset)."""
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    off = int(lib().moe_workspace_accumulator_offset(T, H, I, E, k, wdtype))
+    if off == 0 or off + T * H * 4 > ws.numel():
+        raise ValueError("workspace too small for these sizes")
+    return ws[off:off + T * H * 4].view(torch.float32).view(T, H)
 
 
 def default_workspace(device="cuda") -> Workspace:
@@ -295,6 +318,45 @@ def set_swap_rows(rows_per_expert: int):
 
 def get_swap_rows() -> int:
     return int(lib().moe_get_swap_rows())
+
+
+def set_block_scaled_mma(on: bool):
+    """UE8M0 FP8 experts on the tensor core's block scaling (True, default)
+    or on the software-promotion kernel (False)."""
+    lib().moe_set_block_scaled_mma(1 if on else 0)
+
+
+def get_block_scaled_mma() -> bool:
+    return bool(lib().moe_get_block_scaled_mma())
+
+
+def set_tile_group(m_tiles: int):
+    """m-tiles per tile group of the token-row gate/up GEMM (0: all)."""
+    lib().moe_set_tile_group(int(m_tiles))
+
+
+def get_tile_group() -> int:
+    return int(lib().moe_get_tile_group())
+
+
+def set_decode_single(on: bool):
+    """Small bf16 decode batches (<= 64 routed rows) as one cooperative
+    kernel (True) or as two kernels (False, default)."""
+    lib().moe_set_decode_single(1 if on else 0)
+
+
+def get_decode_single() -> bool:
+    return bool(lib().moe_get_decode_single())
+
+
+def set_fp4_gemv_rows(rows: int):
+    """FP4 forwards with T*k <= rows use the CUDA-core GEMVs, larger ones the
+    block-scaled tensor-core GEMMs (< 0: default 64; 0: GEMMs always)."""
+    lib().moe_set_fp4_gemv_rows(int(rows))
+
+
+def get_fp4_gemv_rows() -> int:
+    return int(lib().moe_get_fp4_gemv_rows())
 
 
 def profile_begin():

@@ -13,12 +13,16 @@
 //                A 16-byte vector of codes is exactly one scale block.
 //   activations  the hidden rows and h are quantised to e4m3 in 1x32 UE8M0
 //                blocks (scale = smallest power of two >= amax/448); the
-//                kernels keep the dequantised values, exact in fp32.
+//                kernels keep the dequantised values, exact in fp32, in eight
+//                "planes" per row (float4 group g of block c at g * C/32 + c),
+//                so that the lanes of a warp, one block each, load 512
+//                contiguous bytes per group.
 //
 //   fp4_quant_x      hidden [T, H] bf16 -> quantised values, fp32 [T, H]
 //   fp4_gate_up      item = (touched expert, 32 features), 8 features per
 //                    warp: gate and up rows streamed once against the
-//                    expert's token rows; h = act(g) * u of the 32 features
+//                    expert's token rows (in chunks of 8, 4, 2, 1 rows, so
+//                    no row is computed twice); h = act(g) * u of the 32 features
 //                    is one 1x32 block per row, quantised in the CTA ->
 //                    fp32 [n, I] in expert-sorted row order
 //   fp4_down         2 output columns per warp: their W_down rows streamed
@@ -26,6 +30,8 @@
 //                    shared memory (ascending expert order), bf16 out
 //   fp4_quantize     offline: bf16 weights -> packed codes + UE8M0 bytes
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "decode_common.cuh"
 
@@ -68,7 +74,9 @@ __device__ __forceinline__ void e2m1x8_to_f32(uint32_t v, float (&f)[8]) {
 
 // acc_a[t] += row_a . x_t and acc_b[t] += row_b . x_t for two packed e2m1
 // rows of nblk 32-element blocks (codes wa/wb, UE8M0 bytes sa/sb) and fp32
-// rows x_t.  Lane handles blocks lane, lane+32, ...; per block the code
+// rows x_t stored in planes: float4 group g (elements 4g..4g+3) of block c
+// at x_t[g * nblk + c].  Lane handles blocks lane, lane+32, ..., so the 32
+// lanes' loads of one group are 512 contiguous bytes; per block the code
 // products are summed first and then scaled once.
 template <int MT>
 __device__ __forceinline__ void fp4_dot2(const uint4* __restrict__ wa, const uint8_t* __restrict__ sa,
@@ -103,8 +111,8 @@ __device__ __forceinline__ void fp4_dot2(const uint4* __restrict__ wa, const uin
         e2m1x8_to_f32(wb4[q], fb);
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
-          const float4 x0 = __ldg(xr[t] + c * 8 + 2 * q);
-          const float4 x1 = __ldg(xr[t] + c * 8 + 2 * q + 1);
+          const float4 x0 = __ldg(xr[t] + (2 * q) * nblk + c);
+          const float4 x1 = __ldg(xr[t] + (2 * q + 1) * nblk + c);
           const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           pa[t] = dot8(fa, xf, pa[t]);
           pb[t] = dot8(fb, xf, pb[t]);
@@ -144,9 +152,10 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
 
 // ------------------------------------------------------------ activations
 // One thread per 1x32 block of hidden: e4m3 codes with a UE8M0 scale, kept
-// as their values (code value * scale, exact in fp32).
+// as their values (code value * scale, exact in fp32), in the plane layout
+// the GEMVs read: row t, block c, group g at xdq[t * H/4 + g * rblk + c].
 __global__ void __launch_bounds__(256) fp4_quant_x_kernel(const uint4* __restrict__ hidden, long nblk,
-                                                          float4* __restrict__ xdq) {
+                                                          int rblk, float4* __restrict__ xdq) {
   pdl_launch_dependents();
   pdl_wait();
   for (long b = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk;
@@ -174,9 +183,11 @@ __global__ void __launch_bounds__(256) fp4_quant_x_kernel(const uint4* __restric
       x[2 * i] = d.x * sc;
       x[2 * i + 1] = d.y * sc;
     }
+    const long t = b / rblk, c = b - t * rblk;
+    float4* row = xdq + t * (rblk * 8);
 #pragma unroll
     for (int i = 0; i < kFp4Block / 4; ++i)
-      xdq[b * 8 + i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      row[i * rblk + c] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
   }
 }
 
@@ -202,37 +213,47 @@ __global__ void __launch_bounds__(128) fp4_gate_up_kernel(
     const int e = tab.te[j];
     const int r0 = tab.tb[j];
     const int m = tab.tb[j + 1] - r0;
-    for (int t0 = 0; t0 < m; t0 += MT) {
-      const float4* xr[MT];
+    // the expert's rows in chunks of 8, 4, 2, 1 (no duplicated rows)
+    auto chunk = [&](auto mt_tag, int t0) {
+      constexpr int C = decltype(mt_tag)::value;
+      const float4* xr[C];
 #pragma unroll
-      for (int t = 0; t < MT; ++t)
+      for (int t = 0; t < C; ++t)
         xr[t] = reinterpret_cast<const float4*>(xdq) +
-                static_cast<long>(tab.sf[r0 + min(t0 + t, m - 1)] / k) * (H / 4);
+                static_cast<long>(tab.sf[r0 + t0 + t] / k) * (H / 4);
       for (int q = 0; q < 8; ++q) {
         const int fl = warp * 8 + q;                              // feature in the block
         const long ga = static_cast<long>(e) * 2 * I + fb * kFp4Block + fl;  // gate row
         const long ua = ga + I;                                   // up row
-        float ag[MT], au[MT];
+        float ag[C], au[C];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) ag[t] = au[t] = 0.f;
-        fp4_dot2<MT>(reinterpret_cast<const uint4*>(wgu + ga * row_bytes), sgu + ga * nblk,
-                     reinterpret_cast<const uint4*>(wgu + ua * row_bytes), sgu + ua * nblk, xr,
-                     nblk, lane, ag, au);
+        for (int t = 0; t < C; ++t) ag[t] = au[t] = 0.f;
+        fp4_dot2<C>(reinterpret_cast<const uint4*>(wgu + ga * row_bytes), sgu + ga * nblk,
+                    reinterpret_cast<const uint4*>(wgu + ua * row_bytes), sgu + ua * nblk, xr,
+                    nblk, lane, ag, au);
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
+        for (int t = 0; t < C; ++t) {
           const float g = warp_sum(ag[t]);
           const float u = warp_sum(au[t]);
-          if (lane == 0 && t0 + t < m) s_h[t0 + t][fl] = gate_act(g, act) * u;
+          if (lane == 0) s_h[t0 + t][fl] = gate_act(g, act) * u;
         }
       }
+    };
+    for (int t0 = 0; t0 < m;) {
+      const int rem = m - t0;
+      if (MT >= 8 && rem >= 8) { chunk(std::integral_constant<int, 8>{}, t0); t0 += 8; }
+      else if (MT >= 4 && rem >= 4) { chunk(std::integral_constant<int, 4>{}, t0); t0 += 4; }
+      else if (MT >= 2 && rem >= 2) { chunk(std::integral_constant<int, 2>{}, t0); t0 += 2; }
+      else { chunk(std::integral_constant<int, 1>{}, t0); t0 += 1; }
     }
     __syncthreads();
-    for (int t = warp; t < m; t += 4) {  // row t's block: lane = feature
+    // row t's block: lane = feature; stored in the plane layout of the down GEMV
+    for (int t = warp; t < m; t += 4) {
       const float v = s_h[t][lane];
       uint32_t stored;
       const float sc = block_scale(warp_absmax(v), true, &stored);
       const float d = e4m3x2_to_f32(e4m3x2(v * (1.0f / sc), 0.f)).x;
-      hq[static_cast<long>(r0 + t) * I + fb * kFp4Block + lane] = d * sc;
+      hq[static_cast<long>(r0 + t) * I + ((lane >> 2) * nfb + fb) * 4 + (lane & 3)] = d * sc;
     }
     __syncthreads();
   }
@@ -264,29 +285,37 @@ __global__ void __launch_bounds__(128) fp4_down_kernel(
       const int r0 = tab.tb[j];
       const int m = tab.tb[j + 1] - r0;
       const long ra = static_cast<long>(e) * H + c;  // W_down rows of columns c, c+1
-      for (int t0 = 0; t0 < m; t0 += MT) {
-        const float4* hr[MT];
+      auto chunk = [&](auto mt_tag, int t0) {
+        constexpr int C = decltype(mt_tag)::value;
+        const float4* hr[C];
 #pragma unroll
-        for (int t = 0; t < MT; ++t)
-          hr[t] = reinterpret_cast<const float4*>(hq) +
-                  static_cast<long>(r0 + min(t0 + t, m - 1)) * (I / 4);
-        float ya[MT], yb[MT];
+        for (int t = 0; t < C; ++t)
+          hr[t] = reinterpret_cast<const float4*>(hq) + static_cast<long>(r0 + t0 + t) * (I / 4);
+        float ya[C], yb[C];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) ya[t] = yb[t] = 0.f;
-        fp4_dot2<MT>(reinterpret_cast<const uint4*>(wd + ra * row_bytes), sd + ra * nblk,
-                     reinterpret_cast<const uint4*>(wd + (ra + 1) * row_bytes), sd + (ra + 1) * nblk,
-                     hr, nblk, lane, ya, yb);
+        for (int t = 0; t < C; ++t) ya[t] = yb[t] = 0.f;
+        fp4_dot2<C>(reinterpret_cast<const uint4*>(wd + ra * row_bytes), sd + ra * nblk,
+                    reinterpret_cast<const uint4*>(wd + (ra + 1) * row_bytes), sd + (ra + 1) * nblk,
+                    hr, nblk, lane, ya, yb);
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
+        for (int t = 0; t < C; ++t) {
           const float a = warp_sum(ya[t]);
           const float b = warp_sum(yb[t]);
-          if (lane == 0 && t0 + t < m) {
+          if (lane == 0) {
             const int f = tab.sf[r0 + t0 + t];
             const float w = __ldg(topk_w + f);
             acc[0][f / k] += a * w;
             acc[1][f / k] += b * w;
           }
         }
+      };
+      // the expert's rows in chunks of 8, 4, 2, 1 (no duplicated rows)
+      for (int t0 = 0; t0 < m;) {
+        const int rem = m - t0;
+        if (MT >= 8 && rem >= 8) { chunk(std::integral_constant<int, 8>{}, t0); t0 += 8; }
+        else if (MT >= 4 && rem >= 4) { chunk(std::integral_constant<int, 4>{}, t0); t0 += 4; }
+        else if (MT >= 2 && rem >= 2) { chunk(std::integral_constant<int, 2>{}, t0); t0 += 2; }
+        else { chunk(std::integral_constant<int, 1>{}, t0); t0 += 1; }
       }
     }
     __syncwarp();
@@ -338,7 +367,9 @@ __global__ void __launch_bounds__(256) fp4_quantize_kernel(const uint4* __restri
   }
 }
 
-int mt_for_fp4(int T) { return T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1; }
+// Largest token chunk the kernels instantiate: chunks of 8 rows spilled
+// registers, so experts with more rows take several chunks of 4.
+int mt_for_fp4(int T) { return T >= 4 ? 4 : T >= 2 ? 2 : 1; }
 
 int grid_for(long items, int num_sms) {
   const long slots = static_cast<long>(num_sms) * 16;
@@ -351,7 +382,8 @@ int grid_for(long items, int num_sms) {
 cudaError_t launch_fp4_quant_x(const Fp4DecodeArgs& a, cudaStream_t s) {
   const long nxb = static_cast<long>(a.T) * (a.H / kFp4Block);
   launch_pdl(fp4_quant_x_kernel, grid_for((nxb + 255) / 256, a.num_sms), 256, 0, s,
-             static_cast<const uint4*>(a.hidden), nxb, reinterpret_cast<float4*>(a.xdq));
+             static_cast<const uint4*>(a.hidden), nxb, a.H / kFp4Block,
+             reinterpret_cast<float4*>(a.xdq));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -362,7 +394,6 @@ cudaError_t launch_fp4_gate_up(const Fp4DecodeArgs& a, cudaStream_t s) {
   const auto* w = static_cast<const uint8_t*>(a.w_gate_up);
   const auto* sc = static_cast<const uint8_t*>(a.scale_gate_up);
   switch (mt_for_fp4(a.T)) {
-    case 8: launch_pdl(fp4_gate_up_kernel<8>, g, 128, 0, s, a.xdq, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.hq, a.err, a.act); break;
     case 4: launch_pdl(fp4_gate_up_kernel<4>, g, 128, 0, s, a.xdq, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.hq, a.err, a.act); break;
     case 2: launch_pdl(fp4_gate_up_kernel<2>, g, 128, 0, s, a.xdq, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.hq, a.err, a.act); break;
     default: launch_pdl(fp4_gate_up_kernel<1>, g, 128, 0, s, a.xdq, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.hq, a.err, a.act); break;
@@ -378,7 +409,6 @@ cudaError_t launch_fp4_down(const Fp4DecodeArgs& a, cudaStream_t s) {
   const auto* sc = static_cast<const uint8_t*>(a.scale_down);
   auto* o = static_cast<__nv_bfloat16*>(a.out);
   switch (mt_for_fp4(a.T)) {
-    case 8: launch_pdl(fp4_down_kernel<8>, g, 128, 0, s, a.hq, a.T, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.topk_w, o, a.err); break;
     case 4: launch_pdl(fp4_down_kernel<4>, g, 128, 0, s, a.hq, a.T, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.topk_w, o, a.err); break;
     case 2: launch_pdl(fp4_down_kernel<2>, g, 128, 0, s, a.hq, a.T, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.topk_w, o, a.err); break;
     default: launch_pdl(fp4_down_kernel<1>, g, 128, 0, s, a.hq, a.T, a.H, a.I, a.k, a.E, n, w, sc, a.topk_idx, a.topk_w, o, a.err); break;

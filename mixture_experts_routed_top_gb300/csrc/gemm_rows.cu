@@ -71,10 +71,16 @@ struct GemmDev {
   const int* sorted_f;
   const float* topk_w;
   int act;             // moe_activation of the gate/up epilogue
+  int group;           // m-tiles per tile group (0: all of the expert's)
 };
 
-__device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* s_pref, int& e,
-                                            int& m, int& n) {
+// Tile -> (expert e, m-tile m, n-tile n).  Inside an expert the m-tiles run
+// in groups of `group`: a group's tiles for every n-tile, m fastest, then
+// the next group.  So CTAs running together share a weight tile through L2
+// (m fastest), and an expert with many m-tiles re-reads only one group's
+// activation tiles per n-tile instead of all of them.
+__device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* s_pref,
+                                            int group, int& e, int& m, int& n) {
   const int v = tile / NT;
   int lo = 0, hi = E;
   while (lo < hi) {  // largest e with s_pref[e] <= v
@@ -85,8 +91,12 @@ __device__ __forceinline__ void decode_tile(int tile, int NT, int E, const int* 
   e = lo;
   const int mt = s_pref[e + 1] - s_pref[e];
   const int local = tile - s_pref[e] * NT;
-  n = local / mt;
-  m = local - n * mt;
+  const int G = (group > 0 && group < mt) ? group : mt;
+  const int g = local / (G * NT);
+  const int gg = min(G, mt - g * G);      // m-tiles in this group
+  const int r = local - g * G * NT;
+  n = r / gg;
+  m = g * G + (r - n * gg);
 }
 
 template <int EPI, int BN, int BK>
@@ -158,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, m, n;
-        decode_tile(tile, NT, E, s_pref, e, m, n);
+        decode_tile(tile, NT, E, s_pref, p.group, e, m, n);
         const int arow = s_off[e] + m * BM;
         const int brow = (EPI == EPI_SWIGLU) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
         for (int kb = 0; kb < KB; ++kb) {
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       int e, m, n;
-      decode_tile(tile, NT, E, s_pref, e, m, n);
+      decode_tile(tile, NT, E, s_pref, p.group, e, m, n);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       int ok = 1;
@@ -349,6 +359,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
   p.act = a.act;
+  p.group = a.tile_group;
   launch_pdl(kern, a.num_sms, kThreads, L::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

@@ -63,6 +63,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // thread may set them while others launch forwards.
 std::atomic<int> g_decode_rows{-1};
 std::atomic<int> g_swap_rows{-1};
+std::atomic<int> g_block_scaled_mma{1};   // UE8M0 FP8 experts on the tensor core's block scaling
+std::atomic<int> g_fp4_gemv_rows{-1};     // FP4: CUDA-core GEMVs up to this many routed rows
+std::atomic<int> g_decode_single{0};      // small decode batches as one cooperative launch
+std::atomic<int> g_tile_group{0};         // token-row gate/up GEMM: m-tiles per tile group
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -92,11 +96,13 @@ WsLayout ws_layout(long T, long H, long I, long E, long k, moe_wdtype wd) {
   L.blk_counts = take(nchunks * E * 4);
   // activations and h: e4m3 codes (FP8), bf16, or the quantised values in
   // fp32 (FP4, which keeps one row per token for the activations)
+  // (FP4 keeps both forms: fp32 values for the small-token GEMVs, e4m3
+  // codes with K-block-major scale words for the block-scaled GEMMs)
   const size_t esz = fp8 ? 1 : fp4 ? 4 : 2;
-  L.xa = take((fp4 ? T : n) * H * esz);
-  L.xa_scale = take(fp8 ? n * scale_stride(H / 128) * 4 : 0);
+  L.xa = take(fp4 ? std::max(T * H * 4, n * H) : n * H * esz);
+  L.xa_scale = take(fp8 ? n * scale_stride(H / 128) * 4 : fp4 ? n * (H / 128) * 4 : 0);
   L.hb = take(n * I * esz);
-  L.hb_scale = take(fp8 ? n * scale_stride(I / 128) * 4 : 0);
+  L.hb_scale = take(fp8 ? n * scale_stride(I / 128) * 4 : fp4 ? n * (I / 128) * 4 : 0);
   L.out32 = take(T * H * 4);
   L.ydec = take(n <= kDecodeRowsMax ? n * H * 4 : 0);
   L.total = align_up(off, 1024);
@@ -145,6 +151,25 @@ moe_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
                   row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+// 2-D packed e2m1 matrix [rows, k_elems] (two codes per byte, row stride
+// k_elems/2 bytes), box 128 elements x 128 rows, expanded by TMA into the
+// one-byte-per-element-slot shared-memory form (16 codes in 8 bytes, 8 bytes
+// of padding) and swizzled at 128 bytes.
+moe_status make_map_e2m1(CUtensorMap* m, const void* base, uint64_t k_elems, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {k_elems, rows};
+  cuuint64_t strides[1] = {k_elems / 2};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (packed e2m1) failed (%d)", (int)r);
   return MOE_OK;
 }
 
@@ -227,6 +252,23 @@ int moe_get_swap_rows(void) {
   return r < 0 ? kSwapRowsDefault : r;
 }
 
+void moe_set_tile_group(int m_tiles) { g_tile_group = m_tiles < 0 ? 0 : m_tiles; }
+int moe_get_tile_group(void) { return g_tile_group.load(std::memory_order_relaxed); }
+
+void moe_set_decode_single(int on) { g_decode_single = on ? 1 : 0; }
+int moe_get_decode_single(void) { return g_decode_single.load(std::memory_order_relaxed); }
+
+void moe_set_block_scaled_mma(int on) { g_block_scaled_mma = on ? 1 : 0; }
+int moe_get_block_scaled_mma(void) { return g_block_scaled_mma.load(std::memory_order_relaxed); }
+
+void moe_set_fp4_gemv_rows(int rows) {
+  g_fp4_gemv_rows = rows < 0 ? -1 : (rows > kFusedDecodeRows ? kFusedDecodeRows : rows);
+}
+int moe_get_fp4_gemv_rows(void) {
+  const int r = g_fp4_gemv_rows.load(std::memory_order_relaxed);
+  return r < 0 ? kFusedDecodeRows : r;
+}
+
 moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                      void* stream) {
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "moe_route: T < 0");
@@ -287,6 +329,11 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, moe_wdtype wdtype) 
   return ws_layout(T, H, I, E, k, wdtype).total;
 }
 
+size_t moe_workspace_accumulator_offset(int T, int H, int I, int E, int k, moe_wdtype wdtype) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  return ws_layout(T, H, I, E, k, wdtype).out32;
+}
+
 moe_status moe_experts_forward(const void* hidden, int T, int H, const int32_t* topk_idx,
                                const float* topk_w, int E, int k, int I, const void* w_gate_up,
                                const void* w_down, moe_wdtype wdtype, const void* scale_gate_up,
@@ -331,10 +378,15 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need UE8M0 block scales");
     if (!scale_gate_up || !scale_down)
       return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need scale buffers");
-    if (static_cast<long>(T) * k > kFusedDecodeRows)
-      return fail(MOE_ERR_UNSUPPORTED,
-                  "moe_experts_forward: FP4 weights run on the small-token path only (T*k <= %d)",
-                  kFusedDecodeRows);
+    if (static_cast<long>(T) * k > moe_get_fp4_gemv_rows()) {
+      if (H % 256)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "moe_experts_forward: FP4 weights above %d routed rows need H %% 256 == 0",
+                    moe_get_fp4_gemv_rows());
+      if (!aligned(w_gate_up, 32) || !aligned(w_down, 32))
+        return fail(MOE_ERR_INVALID_ARG,
+                    "moe_experts_forward: FP4 weights must be 32-byte aligned (packed TMA loads)");
+    }
   } else if (sfmt != MOE_SCALE_NONE || scale_gate_up || scale_down) {
     return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: bf16 weights take no scales");
   }
@@ -372,6 +424,87 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
 
   const int sms = num_sms();
   cudaError_t e;
+  const bool mx = (fp8 && sfmt == MOE_SCALE_UE8M0 && moe_get_block_scaled_mma()) ||
+                  (fp4 && n > moe_get_fp4_gemv_rows());
+  if (mx) {
+    // FP8 (UE8M0) or FP4 experts on the tensor core's block scaling:
+    // dispatch, gather + e4m3 quantisation of the rows in 1x128 (FP8) or 1x32
+    // (FP4) blocks, the two block-scaled grouped GEMMs, bf16 output
+    uint8_t* xq = w + L.xa;
+    uint32_t* xs = reinterpret_cast<uint32_t*>(w + L.xa_scale);
+    uint8_t* hq = w + L.hb;
+    uint32_t* hs = reinterpret_cast<uint32_t*>(w + L.hb_scale);
+    CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
+    moe_status st;
+    if ((st = make_map(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, n)) != MOE_OK) return st;
+    if ((st = make_map(&tm_h, hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, n)) != MOE_OK) return st;
+    if (fp4) {
+      if ((st = make_map_e2m1(&tm_wgu, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+        return st;
+      if ((st = make_map_e2m1(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H)) != MOE_OK)
+        return st;
+    } else {
+      if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H,
+                         static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+        return st;
+      if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I,
+                         static_cast<uint64_t>(E) * H)) != MOE_OK)
+        return st;
+    }
+    {
+      StageScope sc(s, MOE_STAGE_DISPATCH);
+      e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
+                                 : launch_dispatch(topk_idx, T, E, k, d, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dispatch");
+      if ((e = launch_gather_quant_mx(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n),
+                                      fp4 ? 32 : 128, xq, xs, s)) != cudaSuccess)
+        return cuda_fail(e, "gather_quant_mx");
+      if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
+        return cuda_fail(e, "zero out32");
+    }
+    GroupedGemmMxArgs g{};
+    g.offsets = d.offsets;
+    g.tile_pref = d.tile_pref;
+    g.E = E;
+    g.I = I;
+    g.H = H;
+    g.k = k;
+    g.n_rows = static_cast<int>(n);
+    g.err = d.err;
+    g.hq = hq;
+    g.hs = hs;
+    g.out32 = out32;
+    g.sorted_f = d.sorted_f;
+    g.topk_w = topk_w;
+    g.act = static_cast<int>(act);
+    const long mtiles_max = n / kBM + E;
+    {
+      StageScope sc(s, MOE_STAGE_GEMM1);
+      g.tm_a = &tm_x;
+      g.tm_b = &tm_wgu;
+      g.K = H;
+      g.a_sf = xs;
+      g.w_sf = static_cast<const uint8_t*>(scale_gate_up);
+      g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
+      if ((e = launch_gemm1_mx(g, fp4, s)) != cudaSuccess) return cuda_fail(e, "gemm1_mx");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_GEMM2);
+      g.tm_a = &tm_h;
+      g.tm_b = &tm_wd;
+      g.K = I;
+      g.a_sf = hs;
+      g.w_sf = static_cast<const uint8_t*>(scale_down);
+      g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / 256)));
+      if ((e = launch_gemm2_mx(g, fp4, s)) != cudaSuccess) return cuda_fail(e, "gemm2_mx");
+    }
+    {
+      StageScope sc(s, MOE_STAGE_FINISH);
+      if ((e = launch_to_bf16(out32, out, static_cast<long>(T) * H, s)) != cudaSuccess)
+        return cuda_fail(e, "to_bf16");
+    }
+    return MOE_OK;
+  }
   if (fp4) {
     // packed e2m1 weights, small-token path: the routing table is rebuilt
     // in the gate/up and down kernels, and the down kernel combines
@@ -429,6 +562,14 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     a.k = k;
     a.num_sms = sms;
     a.act = static_cast<int>(act);
+    if (decode_fused_fits(a) && g_decode_single.load(std::memory_order_relaxed)) {
+      // one cooperative kernel: gate/up, then down + combine, the down
+      // weights streaming while the last h values are computed
+      StageScope sc(s, MOE_STAGE_GEMM1);
+      e = launch_decode_single(a, topk_idx, d.err, s);
+      if (e == cudaSuccess) return MOE_OK;
+      (void)cudaGetLastError();   // not launched (grid too large for this GPU): two kernels
+    }
     if (decode_fused_fits(a)) {
       // routing table rebuilt inside both kernels; the down kernel combines
       {
@@ -593,6 +734,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     g.tm_b = swap1 ? &tm_x : &tm_wgu;
     g.K = H;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
+    g.tile_group = moe_get_tile_group();
     e = swap1 ? launch_gemm1_bf16_swap(g, s) : launch_gemm1_bf16_rows(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm1");
   }
@@ -655,8 +797,10 @@ moe_status moe_workspace_status(void* ws, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_workspace_status");
   if (err) {
-    const int zero = 0;
-    e = cudaMemcpyAsync(ws, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+    // the error word and the decode counters (which a timed-out launch may
+    // have left non-zero) start again from zero
+    const int zero[3] = {0, 0, 0};
+    e = cudaMemcpyAsync(ws, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_workspace_status clear");
     if (err & (ERR_TIMEOUT_PRODUCER | ERR_TIMEOUT_MMA | ERR_TIMEOUT_EPILOGUE | ERR_TIMEOUT_SELFTEST))

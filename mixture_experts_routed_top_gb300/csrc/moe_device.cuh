@@ -182,6 +182,64 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA: fp32 D,
+// K-major A and B in the formats a_fmt / b_fmt (kMxE4M3, kMxE2M1), UE8M0
+// scale factors, and sf_id = which byte of each operand's 32-bit scale word
+// (that is, which 32-wide K sub-block of a 128-wide K block) this
+// instruction applies.
+constexpr uint32_t kMxE4M3 = 0, kMxE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t a_fmt, uint32_t b_fmt,
+                                                uint32_t sf_id) {
+  return (sf_id << 4)                                // B scale-factor byte
+         | (a_fmt << 7)                              // A format
+         | (b_fmt << 10)                             // B format
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale factors are UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (sf_id << 29);                            // A scale-factor byte
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte tile without swizzling
+// (8-row core matrices of 128 bytes, stored one after the other): the
+// source of a scale-factor copy into TMEM.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address / 16
+  d |= static_cast<uint64_t>(128 >> 4) << 16;            // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;            // stride byte offset: next 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (sm_100 family)
+  return d;                                              // swizzle mode 0: none
+}
+
+// Warp-independent (one thread): copy a 32-row x 16-byte scale-factor tile
+// from shared memory into TMEM columns taddr..taddr+3, lanes 0..31, and the
+// same data into each of the other three lane quarters.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Block-scaled D[tmem] (+)= (A * sfA) (B * sfB)^T, single CTA, K = 32 per
+// instruction, scale factors read from TMEM (one byte per row of A and per
+// column of B, selected by the descriptor's sf_id).
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tcgen05.cp, TMA) before another thread hands them over.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, single CTA.
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {

@@ -55,11 +55,15 @@ inline long dispatch_chunk(long n) {
 constexpr int kSmallDispatchMax = 2048;  // T*k at or below: one-CTA dispatch
 constexpr int kBM = 128;               // max token rows per grouped-GEMM tile
 
-// Device-side error word block at the head of every workspace.
+// Device-side word block at the head of every workspace: the error word,
+// then the two counters the single-launch decode kernel synchronises its
+// CTAs with (zero between launches; the last CTA of a launch resets them).
 struct WsHeader {
   int err;
   int pad[63];
 };
+constexpr int kSyncArriveWord = 1;
+constexpr int kSyncDoneWord = 2;
 
 // Pointers into the dispatch part of a workspace.
 struct DispatchBufs {
@@ -124,6 +128,7 @@ struct GroupedGemmArgs {
   const float* topk_w;
   int num_sms;
   int act;                   // moe_activation of the gate/up epilogue
+  int tile_group = 0;        // token-row kernel: m-tiles per tile group (0: all)
 };
 cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
@@ -153,6 +158,37 @@ struct GroupedGemmFp8Args {
 };
 cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
 cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
+
+// Block-scaled grouped GEMMs on the tensor core's UE8M0 block scaling
+// (tcgen05.mma kind::mxf8f6f4, token rows as M, N = 256): FP8 experts with
+// UE8M0 128x128 weight scales, and FP4 (e2m1) experts with 1x32 weight
+// scales.  Activations are e4m3 with one 32-bit scale word per row and
+// 128-wide K block (byte j = the exponent of 32-wide sub-block j), stored
+// K-block-major: a_sf[kb * n_rows + row].
+struct GroupedGemmMxArgs {
+  const CUtensorMap* tm_a;   // e4m3 activations [n_rows, K], box 128 x 128 B
+  const CUtensorMap* tm_b;   // weights [E * Nw, K]: e4m3 (uint8 map) or e2m1 (16U4_ALIGN16B map)
+  const int* offsets;
+  const int* tile_pref;
+  int E, K, I, H, k, n_rows;
+  int* err;
+  const uint32_t* a_sf;      // [K/128][n_rows]
+  const uint8_t* w_sf;       // FP8: [E, Nw/128, K/128]; FP4: [E * Nw, K/32]
+  uint8_t* hq;               // gate/up output codes [n_rows, I]
+  uint32_t* hs;              // gate/up output scale words [I/128][n_rows]
+  float* out32;              // down output accumulator [T, H]
+  const int* sorted_f;
+  const float* topk_w;
+  int num_sms;
+  int act;
+};
+cudaError_t launch_gemm1_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
+cudaError_t launch_gemm2_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
+// Gather + e4m3 quantisation of the routed rows in 1 x block UE8M0 blocks
+// (block 128 or 32), scale words K-block-major as above.
+cudaError_t launch_gather_quant_mx(const void* hidden, int H, int k, const int* sorted_f,
+                                   const int* nvalid, int rows, int block, uint8_t* xq,
+                                   uint32_t* xs, cudaStream_t s);
 
 // Small-token decode path.
 struct DecodeArgs {
@@ -184,6 +220,11 @@ cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk
                                        cudaStream_t s);
 cudaError_t launch_decode_fused_down(const DecodeArgs& a, const int32_t* topk_idx, int* err,
                                      cudaStream_t s);
+// Both fused decode kernels as one cooperative launch (phase B's W_down
+// stream overlaps phase A); head = the workspace's word block.  Returns an
+// error without launching when the GPU cannot hold the grid at once.
+cudaError_t launch_decode_single(const DecodeArgs& a, const int32_t* topk_idx, int* head,
+                                 cudaStream_t s);
 
 // FP4 (e2m1, 1x32 UE8M0 blocks) experts, small-token path only:
 // T*k <= kFusedDecodeRows.  Three kernels: activation quantisation, gate/up

@@ -15,9 +15,19 @@ whose k experts all lie in that set are used, taking the eligible row
 nearest each tile edge; this bounds how many experts the oracle has to
 dequantise.
 
-Test infrastructure: uses the oracle, never the CUDA library.
+The check itself is made on the fp32 accumulator the grouped paths sum
+into (read back from the workspace): it must be within the tolerance of the
+oracle, and the bf16 output must be exactly its round-to-nearest-even image.
+Comparing the bf16 output with the oracle directly would also charge the
+output's own rounding to the kernels: at millions of outputs the largest
+reach several times rms, where half a bf16 unit (up to 2^-8 of the value)
+alone approaches 2e-2 of rms.
+
+Test infrastructure: uses the oracle and the library's binding, never the
+library's arithmetic.
 """
 import numpy as np
+import torch
 
 import oracle as O
 
@@ -99,3 +109,20 @@ def fp8_expert_fn(q_gate_up, s_gate_up, q_down, s_down, fmt):
                              q_gate_up[sl].cpu().numpy(), s_gate_up[sl].cpu().numpy(),
                              q_down[sl].cpu().numpy(), s_down[sl].cpu().numpy(), fmt)
     return fn
+
+
+def check_accumulator(moe, out, toks, ref, shape, wdtype, tol, workspace=None):
+    """The fp32 accumulator rows of the sampled tokens are within ``tol``
+    (max |err| / rms) of the oracle, and out holds their bf16 RNE images.
+    Returns (accumulator error, bf16 output error against the rounded
+    oracle) for the message of a failing assertion."""
+    ws = moe.default_workspace() if workspace is None else workspace
+    acc = moe.accumulator(ws, shape.T, shape.H, shape.I, shape.E, shape.k, wdtype)
+    tt = torch.from_numpy(np.asarray(toks)).to(out.device)
+    acc_s = acc[tt].cpu().numpy()
+    got = out[tt].float().cpu().numpy()
+    err_acc = O.rel_max_err(acc_s, ref)
+    err_out = O.rel_max_err(got, O.round_to_bf16(ref))
+    assert np.array_equal(got, O.round_to_bf16(acc_s)), "bf16 output is not the RNE image of the accumulator"
+    assert err_acc <= tol, (err_acc, err_out)
+    return err_acc, err_out

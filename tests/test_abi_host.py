@@ -86,9 +86,23 @@ def test_fp4_argument_errors_without_device(L):
     assert b"UE8M0" in L.moe_last_error()
     # ... and need both scale buffers
     assert f(p, 4, 128, p, p, 8, 2, 128, p, p, 2, nul, p, 2, p, p, 1 << 30, nul) == 1
-    # only the small-token path exists for FP4: T*k <= 64
+    # above 64 routed rows FP4 runs on the block-scaled tensor-core GEMMs,
+    # whose 256-wide down tiles need H % 256 == 0 ...
     assert f(p, 33, 128, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 1 << 30, nul) == 2
-    assert b"T*k" in L.moe_last_error()
+    assert b"H % 256" in L.moe_last_error()
+    # ... and 32-byte aligned packed weights (TMA of packed e2m1)
+    p16 = ctypes.c_void_p((1 << 20) + 16)
+    assert f(p, 33, 256, p, p, 8, 2, 128, p16, p, 2, p, p, 2, p, p, 1 << 30, nul) == 1
+    assert b"32-byte" in L.moe_last_error()
+    assert f(p, 33, 256, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 16, nul) == 5
+    # with the GEMV threshold at 0 even one routed row takes the GEMM path
+    L.moe_set_fp4_gemv_rows(0)
+    try:
+        assert L.moe_get_fp4_gemv_rows() == 0
+        assert f(p, 1, 128, p, p, 8, 1, 128, p, p, 2, p, p, 2, p, p, 1 << 30, nul) == 2
+    finally:
+        L.moe_set_fp4_gemv_rows(-1)
+    assert L.moe_get_fp4_gemv_rows() == 64
     # T*k = 64 passes those checks and stops at the workspace size
     assert f(p, 32, 128, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 16, nul) == 5
     need = L.moe_workspace_size(32, 128, 128, 8, 2, 2)
@@ -97,6 +111,18 @@ def test_fp4_argument_errors_without_device(L):
     assert L.moe_quantize_fp4_blocks(nul, 1, 4, 48, nul, nul, nul) == 2    # cols % 32
     assert L.moe_quantize_fp4_blocks(nul, 1, 4, 64, nul, nul, nul) == 1    # null pointers
     assert L.moe_quantize_fp4_blocks(nul, 0, 4, 64, nul, nul, nul) == 0    # empty
+
+
+def test_block_scaled_mma_setting_and_accumulator_offset(L):
+    assert L.moe_get_block_scaled_mma() == 1
+    L.moe_set_block_scaled_mma(0)
+    assert L.moe_get_block_scaled_mma() == 0
+    L.moe_set_block_scaled_mma(1)
+    for wd in (0, 1, 2):
+        off = L.moe_workspace_accumulator_offset(300, 256, 128, 8, 2, wd)
+        assert off % 1024 == 0 and 0 < off
+        assert off + 300 * 256 * 4 <= L.moe_workspace_size(300, 256, 128, 8, 2, wd)
+    assert L.moe_workspace_accumulator_offset(-1, 256, 128, 8, 2, 0) == 0
 
 
 def test_decode_rows_setting(L):

@@ -8,7 +8,8 @@ oracle.
   and of h): max|err| / rms(ref) <= 6e-2, the tolerance used for the FP8
   experts.  Remaining differences come from fp32 accumulation order
   flipping an e4m3 rounding (or a block scale) of h.
-* Only the small-token path exists for this format: T*k <= 64.
+* These shapes run on the small-token GEMVs (T*k <= 64); larger batches run
+  on the block-scaled tensor-core GEMMs (tests/test_gpu_block_scaled.py).
 """
 import numpy as np
 import pytest
@@ -172,10 +173,15 @@ def test_forward_fp4_rejections(moe):
     with pytest.raises(moe.MoEError) as ei:                 # scales missing
         moe.experts_forward(d["hidden"], idx, w, qgu, qd)
     assert ei.value.status == 1
-    big = make_inputs(MoEShape(T=40, H=256, I=128, E=4, k=2), seed=1, device="cuda")
+    # above 64 routed rows the block-scaled GEMMs run; their 256-wide down
+    # tiles need H % 256 == 0
+    narrow = MoEShape(T=40, H=128, I=128, E=4, k=2)
+    big = make_inputs(narrow, seed=1, device="cuda")
     bidx, bw = moe.route(big["logits"], 2)
-    with pytest.raises(moe.MoEError) as ei:                 # T*k = 80 > 64
-        moe.experts_forward(big["hidden"], bidx, bw, qgu, qd, scale_gate_up=sgu, scale_down=sd)
+    nq, ns = moe.quantize_fp4_blocks(big["w_gate_up"])
+    nqd, nsd = moe.quantize_fp4_blocks(big["w_down"])
+    with pytest.raises(moe.MoEError) as ei:                 # T*k = 80 > 64, H = 128
+        moe.experts_forward(big["hidden"], bidx, bw, nq, nqd, scale_gate_up=ns, scale_down=nsd)
     assert ei.value.status == 2
 
 

@@ -144,7 +144,7 @@ def test_forward_fp8_full_size_every_tile(moe, T, fmt):
     first and last token of the other popular experts, using only tokens
     whose eight experts are all among the 16 most popular (more if some tile
     has no such token), so that few experts are dequantised on the host."""
-    from full_size_sampling import fp8_expert_fn, oracle_on_tokens, probe_tokens
+    from full_size_sampling import check_accumulator, fp8_expert_fn, oracle_on_tokens, probe_tokens
     shape = shape_for("dsv3_fp8", T)
     d = make_inputs(shape, seed=0, device="cuda")
     qgu, sgu = moe.quantize_fp8_blocks(d["w_gate_up"], fmt)
@@ -170,5 +170,4 @@ def test_forward_fp8_full_size_every_tile(moe, T, fmt):
     tt = torch.from_numpy(toks).cuda()
     ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
                            fp8_expert_fn(qgu, sgu, qd, sd, fmt))
-    got = out[tt].float().cpu().numpy()
-    assert O.rel_max_err(got, ref) <= FP8_TOL
+    check_accumulator(moe, out, toks, ref, shape, moe.W_FP8_E4M3, FP8_TOL)

@@ -168,13 +168,20 @@ def test_forward_bf16_one_expert_takes_all(moe, path):
     MoEShape(T=4, H=2048, I=1408, E=60, k=4),      # Qwen width at the default threshold
     MoEShape(T=8, H=256, I=2048, E=8, k=4),        # the widest h rows (2048) at 8 tokens per expert
 ])
-def test_forward_bf16_fused_decode(moe, shape, path):
-    """Few routed rows: the two fused decode kernels run (two launches, no
-    dispatch or combine kernel), including the widest rows and the most
-    tokens per expert they see."""
-    n0 = moe.launch_count()
-    out, ref = _forward_case(moe, shape)
-    assert moe.launch_count() - n0 == 2
+@pytest.mark.parametrize("single", [True, False], ids=["one_kernel", "two_kernels"])
+def test_forward_bf16_fused_decode(moe, shape, path, single):
+    """Few routed rows: the routing table is rebuilt inside the kernels, so
+    no dispatch or combine kernel runs: one cooperative kernel (gate/up,
+    then down + combine) or the two fused kernels, including the widest
+    rows and the most tokens per expert they see."""
+    moe.set_decode_single(single)
+    try:
+        n0 = moe.launch_count()
+        out, ref = _forward_case(moe, shape)
+        launches = moe.launch_count() - n0
+    finally:
+        moe.set_decode_single(False)
+    assert launches == (1 if single else 2)
     assert O.rel_max_err(out, ref) <= BF16_TOL
 
 
@@ -298,8 +305,11 @@ def test_forward_bf16_full_size_every_tile(moe, name, T):
     """Full workload size on the GPU, through the default path choice; the
     oracle recomputes the tokens at the edges of every grouped-GEMM tile of
     the busiest expert (63 tiles of 128 rows for the skewed DeepSeek-V3
-    layer) and the first and last token of every other touched expert."""
-    from full_size_sampling import bf16_expert_fn, oracle_on_tokens, probe_tokens
+    layer) and the first and last token of every other touched expert.  The
+    fp32 accumulator is checked against it, and the bf16 output against the
+    accumulator (bit for bit)."""
+    from full_size_sampling import (bf16_expert_fn, check_accumulator, oracle_on_tokens,
+                                    probe_tokens)
     shape = shape_for(name, T)
     d = make_inputs(shape, seed=0, device="cuda")
     idx, w = moe.route(d["logits"], shape.k)
@@ -314,8 +324,7 @@ def test_forward_bf16_full_size_every_tile(moe, name, T):
     tt = torch.from_numpy(toks).cuda()
     ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
                            bf16_expert_fn(d["w_gate_up"], d["w_down"]))
-    got = out[tt].float().cpu().numpy()
-    assert O.rel_max_err(got, ref) <= BF16_TOL
+    check_accumulator(moe, out, toks, ref, shape, moe.W_BF16, BF16_TOL)
 
 
 def _replay_case(moe, shape, seeds, fp8=None):
@@ -370,14 +379,55 @@ def _replay_case(moe, shape, seeds, fp8=None):
 ], indirect=["path"])
 def test_graph_replay_matches_oracle(moe, shape, path):
     """What the benchmark times: the whole step as a replayed CUDA graph,
-    every kernel chained by programmatic dependent launch.  Each replay's
-    output (after new inputs were copied into the captured buffers) must
-    match the oracle on those inputs."""
+    every kernel chained by programmatic dependent launch (the small decode
+    batch as one cooperative kernel).  Each replay's output (after new
+    inputs were copied into the captured buffers) must match the oracle on
+    those inputs."""
     n = 0
     for got, ref in _replay_case(moe, shape, seeds=(20, 21, 22)):
         assert O.rel_max_err(got, ref) <= BF16_TOL
         n += 1
     assert n == 2
+
+
+def test_decode_single_kernel_repeats_and_recovers(moe):
+    """The one-kernel decode path synchronises its CTAs through two counters
+    in the workspace head, which every launch leaves at zero: many launches
+    in a row on one workspace (eager and replayed) all give the oracle's
+    output, and the counters read zero afterwards."""
+    shape = MoEShape(T=1, H=2048, I=1408, E=60, k=4)
+    d = make_inputs(shape, seed=9, device="cuda")
+    idx, w = moe.route(d["logits"], shape.k)
+    ws = moe.Workspace("cuda")
+    moe.set_decode_single(True)
+    out = torch.empty(1, shape.H, dtype=torch.bfloat16, device="cuda")
+    run = lambda: moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"], out=out,
+                                      workspace=ws)
+    outs = []
+    for _ in range(20):
+        run()
+        outs.append(out.clone())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    moe.set_decode_single(False)
+    moe.workspace_status(ws)
+    head = ws.buf[:16].view(torch.int32).cpu().tolist()
+    assert head[:3] == [0, 0, 0]
+    ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
+    experts = np.unique(ref_idx)
+    remap = np.full(shape.E, -1, np.int64)
+    remap[experts] = np.arange(len(experts))
+    et = torch.from_numpy(experts).long().cuda()
+    ref = O.forward(d["hidden"].float().cpu().numpy(), remap[ref_idx].astype(np.int32), ref_w,
+                    d["w_gate_up"].index_select(0, et).float().cpu().numpy(),
+                    d["w_down"].index_select(0, et).float().cpu().numpy())
+    for o in outs + [out]:
+        assert torch.equal(o, outs[0])               # fixed summation order: bit-identical
+    assert O.rel_max_err(out.float().cpu().numpy(), ref) <= BF16_TOL
 
 
 @pytest.mark.parametrize("fmt", ["f32", "ue8m0"])
