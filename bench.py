@@ -351,6 +351,8 @@ def run_ours(args, rank, world, local_rank):
     moe.set_block_scaled_mma(args.ue8m0_kernel == "block-scaled")
     if args.tile_group is not None:
         moe.set_tile_group(args.tile_group)
+    if args.fp4_gemv_rows is not None:
+        moe.set_fp4_gemv_rows(args.fp4_gemv_rows)
     if args.decode_kernels is not None:
         moe.set_decode_single(args.decode_kernels == 1)
     w = build_workload(args.workload, dev)
@@ -688,6 +690,8 @@ def main():
     ap.add_argument("--ue8m0-kernel", default="block-scaled", choices=["block-scaled", "promotion"],
                     help="FP8 experts with UE8M0 scales: tensor-core block scaling (library "
                          "default) or the software promotion kernel")
+    ap.add_argument("--fp4-gemv-rows", type=int, default=None,
+                    help="FP4 routed rows at or below which the GEMVs run (library default 64)")
     ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],
                     help="small bf16 decode batches as one cooperative kernel or two kernels "
                          "(library default)")

@@ -39,7 +39,7 @@
 //               mbarrier; 1x32 blocks for FP4) and written with its scale
 //               words for the down GEMM
 //     down:     y scaled by the routing weight and added into the fp32
-//               output row of the token (vector atomics)
+//               output row of the token (vector reductions)
 // Every mbarrier wait is bounded; on expiry the kernel flags the error word,
 // lets the other roles drain, frees its TMEM and returns.
 #include <atomic>
@@ -460,10 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + 128 * half;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            atomicAdd(reinterpret_cast<float4*>(orow + 4 * j),
-                      make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
-                                  wgt * __uint_as_float(v[4 * j + 2]),
-                                  wgt * __uint_as_float(v[4 * j + 3])));
+            red_add_v4(orow + 4 * j, wgt * __uint_as_float(v[4 * j]),
+                       wgt * __uint_as_float(v[4 * j + 1]), wgt * __uint_as_float(v[4 * j + 2]),
+                       wgt * __uint_as_float(v[4 * j + 3]));
         }
       }
     }

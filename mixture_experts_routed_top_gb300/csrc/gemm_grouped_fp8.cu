@@ -24,7 +24,7 @@
 //                warpgroups exchange their row maxima through shared memory)
 //     down:      warpgroup g owns output columns 64g..64g+63 (inside weight
 //                block row g/2); at tile end y * routing weight is added into
-//                the fp32 accumulator of the token (vector atomics)
+//                the fp32 accumulator of the token (vector reductions)
 // All waits are bounded as in the bf16 kernel.
 #include <cuda_fp8.h>
 
@@ -433,14 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + col0;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            atomicAdd(reinterpret_cast<float4*>(orow + 4 * j),
-                      make_float4(wgt * acc0[4 * j], wgt * acc0[4 * j + 1], wgt * acc0[4 * j + 2],
-                                  wgt * acc0[4 * j + 3]));
+            red_add_v4(orow + 4 * j, wgt * acc0[4 * j], wgt * acc0[4 * j + 1],
+                       wgt * acc0[4 * j + 2], wgt * acc0[4 * j + 3]);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            atomicAdd(reinterpret_cast<float4*>(orow + 32 + 4 * j),
-                      make_float4(wgt * acc1[4 * j], wgt * acc1[4 * j + 1], wgt * acc1[4 * j + 2],
-                                  wgt * acc1[4 * j + 3]));
+            red_add_v4(orow + 32 + 4 * j, wgt * acc1[4 * j], wgt * acc1[4 * j + 1],
+                       wgt * acc1[4 * j + 2], wgt * acc1[4 * j + 3]);
         }
       }
     }

@@ -20,7 +20,7 @@
 //                    is up; h = act(gate) * up stored as bf16 (act: silu,
 //                    exact GELU or relu, uniform over the launch)
 //     down GEMM:     y scaled by the row's routing weight and added (fp32
-//                    vector atomics) into out32[token] - the combine
+//                    vector reductions) into out32[token] - the combine
 // Every mbarrier wait is bounded; on expiry the kernel flags the error word,
 // lets the other roles drain, frees its TMEM and returns.
 #include <atomic>
@@ -309,11 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              float4 a4 = make_float4(wgt * __uint_as_float(v[4 * j]),
-                                      wgt * __uint_as_float(v[4 * j + 1]),
-                                      wgt * __uint_as_float(v[4 * j + 2]),
-                                      wgt * __uint_as_float(v[4 * j + 3]));
-              atomicAdd(reinterpret_cast<float4*>(orow + c * 32 + 4 * j), a4);
+              red_add_v4(orow + c * 32 + 4 * j, wgt * __uint_as_float(v[4 * j]),
+                         wgt * __uint_as_float(v[4 * j + 1]), wgt * __uint_as_float(v[4 * j + 2]),
+                         wgt * __uint_as_float(v[4 * j + 3]));
             }
           }
         }

@@ -17,7 +17,7 @@
 //   silu, exact GELU or relu, uniform over the launch).
 // Down GEMM: boxes = 256 (or 128) consecutive rows of W_down[e]; the
 //   epilogue adds topk_w * D[f, t] into the fp32 accumulator row of the
-//   token (coalesced fp32 atomics across the warp's 32 features).
+//   token (fp32 reductions, coalesced across the warp's 32 features).
 //
 // One persistent CTA per SM, six warps: warp 0 TMA producer (4-stage ring of
 // 48 KB),
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float w = __shfl_sync(0xffffffffu, w_l, i);
             if (i < cnt) {
               float* orow = p.out32 + static_cast<long>(tok) * p.H + col;
-              atomicAdd(orow, w * __uint_as_float(d0[i]));
-              if (NA == 2) atomicAdd(orow + 128, w * __uint_as_float(d1[i]));
+              red_add_f32(orow, w * __uint_as_float(d0[i]));
+              if (NA == 2) red_add_f32(orow + 128, w * __uint_as_float(d1[i]));
             }
           }
         }

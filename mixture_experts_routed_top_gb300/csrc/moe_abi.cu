@@ -66,7 +66,7 @@ std::atomic<int> g_swap_rows{-1};
 std::atomic<int> g_block_scaled_mma{1};   // UE8M0 FP8 experts on the tensor core's block scaling
 std::atomic<int> g_fp4_gemv_rows{-1};     // FP4: CUDA-core GEMVs up to this many routed rows
 std::atomic<int> g_decode_single{0};      // small decode batches as one cooperative launch
-std::atomic<int> g_tile_group{0};         // token-row gate/up GEMM: m-tiles per tile group
+std::atomic<int> g_tile_group{-1};        // token-row gate/up GEMM: m-tiles per tile group
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -252,8 +252,11 @@ int moe_get_swap_rows(void) {
   return r < 0 ? kSwapRowsDefault : r;
 }
 
-void moe_set_tile_group(int m_tiles) { g_tile_group = m_tiles < 0 ? 0 : m_tiles; }
-int moe_get_tile_group(void) { return g_tile_group.load(std::memory_order_relaxed); }
+void moe_set_tile_group(int m_tiles) { g_tile_group = m_tiles < 0 ? -1 : m_tiles; }
+int moe_get_tile_group(void) {
+  const int g = g_tile_group.load(std::memory_order_relaxed);
+  return g < 0 ? kTileGroupDefault : g;
+}
 
 void moe_set_decode_single(int on) { g_decode_single = on ? 1 : 0; }
 int moe_get_decode_single(void) { return g_decode_single.load(std::memory_order_relaxed); }

@@ -119,6 +119,14 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) from global memory into L2 (p and bytes
+// multiples of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -345,6 +353,17 @@ __device__ __forceinline__ float block_scale(float amax, bool ue8m0, uint32_t* s
 // the low byte.
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Fire-and-forget fp32 reductions into global memory (no value returned,
+// so the L2 answers nothing back): the combine of the down projections.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -136,6 +136,7 @@ cudaError_t launch_gemm1_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
+constexpr int kTileGroupDefault = 4;   // token-row gate/up: m-tiles per tile group (measured)
 
 // FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
 struct GroupedGemmFp8Args {
