@@ -135,11 +135,12 @@ size_t moe_workspace_accumulator_offset(int T, int H, int I, int E, int k, moe_w
  *               along the contraction axis: scale_gate_up [E, 2I, H/32],
  *               scale_down [E, H, I/32]; sfmt must be MOE_SCALE_UE8M0.  The
  *               hidden rows and the SwiGLU output are quantised on the fly to
- *               e4m3 in 1x32 UE8M0 blocks.  Up to 64 routed rows (T*k, see
- *               moe_set_fp4_gemv_rows) CUDA-core GEMVs stream the packed
- *               weights; above that block-scaled tensor-core GEMMs run, which
- *               need H % 256 == 0 (else MOE_ERR_UNSUPPORTED) and 32-byte
- *               aligned weight buffers (else MOE_ERR_INVALID_ARG).
+ *               e4m3 in 1x32 UE8M0 blocks.  Block-scaled tensor-core GEMMs
+ *               run these forwards (they need H % 256 == 0 and 32-byte
+ *               aligned weight buffers, else MOE_ERR_UNSUPPORTED /
+ *               MOE_ERR_INVALID_ARG); CUDA-core GEMVs take batches of at most
+ *               64 routed rows when H % 256 != 0, or up to the threshold
+ *               moe_set_fp4_gemv_rows sets.
  *   out         device bf16 [T, H]: out[t] = sum_j topk_w[t,j] *
  *               down(silu(gate x_t) * up x_t) of expert topk_idx[t,j],
  *               accumulated in fp32 and rounded once to bf16
@@ -297,9 +298,10 @@ int moe_get_block_scaled_mma(void);
 /*
  * moe_set_fp4_gemv_rows - FP4 forwards with T*k <= rows run on the
  * CUDA-core GEMVs (small-token path), larger ones on the block-scaled
- * tensor-core GEMMs.  rows < 0 restores the default (64, also the maximum);
- * 0 sends every FP4 forward to the tensor-core GEMMs.  Process-wide;
- * moe_get_fp4_gemv_rows returns the threshold in use.
+ * tensor-core GEMMs.  rows < 0 restores the default (0: the GEMMs at every
+ * size, measured faster than the GEMVs down to one token); values are
+ * clamped to 64.  Process-wide; moe_get_fp4_gemv_rows returns the threshold
+ * in use.
  */
 void moe_set_fp4_gemv_rows(int rows);
 int moe_get_fp4_gemv_rows(void);

@@ -351,7 +351,8 @@ def get_decode_single() -> bool:
 
 def set_fp4_gemv_rows(rows: int):
     """FP4 forwards with T*k <= rows use the CUDA-core GEMVs, larger ones the
-    block-scaled tensor-core GEMMs (< 0: default 64; 0: GEMMs always)."""
+    block-scaled tensor-core GEMMs (< 0: the default, 0 = GEMMs always; at
+    most 64)."""
     lib().moe_set_fp4_gemv_rows(int(rows))
 
 

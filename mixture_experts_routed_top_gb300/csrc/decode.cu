@@ -271,31 +271,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __res
 template <int MT>
 __global__ void __launch_bounds__(128) decode_fused_gate_up_kernel(
     const __nv_bfloat16* __restrict__ hidden, int H, int I, int k, int E, int n,
-    const __nv_bfloat16* __restrict__ wgu, const __nv_bfloat16* __restrict__ wd,
-    const int32_t* __restrict__ topk_idx, __nv_bfloat16* __restrict__ h_out, int* err, int act) {
+    const __nv_bfloat16* __restrict__ wgu, const int32_t* __restrict__ topk_idx,
+    __nv_bfloat16* __restrict__ h_out, int* err, int act) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ SmallTable tab;
   build_small_table(topk_idx, n, E, tab, err);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The touched experts' W_down is fetched into L2 while this kernel streams
-  // W_gate_up (each CTA takes an equal slice, bulk L2 prefetches of at most
-  // 64 KB), so the down GEMV that follows reads it from L2.
-  if (threadIdx.x == 0) {
-    const long per_e = static_cast<long>(H) * I * 2;
-    const long total = per_e * tab.nt;
-    const long chunk = ((total + gridDim.x - 1) / gridDim.x + 15) & ~15L;
-    long b = static_cast<long>(blockIdx.x) * chunk;
-    const long end = min(b + chunk, total);
-    while (b < end) {
-      const int j = static_cast<int>(b / per_e);
-      const long off = b - j * per_e;
-      const long len = min(min(end - b, per_e - off), 65536L);
-      prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(wd) + tab.te[j] * per_e + off,
-                       static_cast<uint32_t>(len));
-      b += len;
-    }
-  }
   const int per_e = I / 4;
   const int n_items = tab.nt * per_e;
   const int H8 = H / 8;
@@ -435,10 +417,10 @@ cudaError_t launch_decode_fused_gate_up(const DecodeArgs& a, const int32_t* topk
   auto* hid = static_cast<const __nv_bfloat16*>(a.hidden);
   auto* w = static_cast<const __nv_bfloat16*>(a.w_gate_up);
   switch (mt_for(a.T)) {
-    case 8: launch_pdl(decode_fused_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, static_cast<const __nv_bfloat16*>(a.w_down), topk_idx, hb, err, a.act); break;
-    case 4: launch_pdl(decode_fused_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, static_cast<const __nv_bfloat16*>(a.w_down), topk_idx, hb, err, a.act); break;
-    case 2: launch_pdl(decode_fused_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, static_cast<const __nv_bfloat16*>(a.w_down), topk_idx, hb, err, a.act); break;
-    default: launch_pdl(decode_fused_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, static_cast<const __nv_bfloat16*>(a.w_down), topk_idx, hb, err, a.act); break;
+    case 8: launch_pdl(decode_fused_gate_up_kernel<8>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    case 4: launch_pdl(decode_fused_gate_up_kernel<4>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    case 2: launch_pdl(decode_fused_gate_up_kernel<2>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
+    default: launch_pdl(decode_fused_gate_up_kernel<1>, grid, 128, 0, s, hid, a.H, a.I, a.k, a.E, n, w, topk_idx, hb, err, a.act); break;
   }
   count_launches(1);
   return cudaGetLastError();

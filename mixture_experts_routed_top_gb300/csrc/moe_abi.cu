@@ -269,7 +269,7 @@ void moe_set_fp4_gemv_rows(int rows) {
 }
 int moe_get_fp4_gemv_rows(void) {
   const int r = g_fp4_gemv_rows.load(std::memory_order_relaxed);
-  return r < 0 ? kFusedDecodeRows : r;
+  return r < 0 ? kFp4GemvRowsDefault : r;
 }
 
 moe_status moe_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
@@ -381,11 +381,12 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need UE8M0 block scales");
     if (!scale_gate_up || !scale_down)
       return fail(MOE_ERR_INVALID_ARG, "moe_experts_forward: FP4 weights need scale buffers");
-    if (static_cast<long>(T) * k > moe_get_fp4_gemv_rows()) {
+    if (static_cast<long>(T) * k > moe_get_fp4_gemv_rows() &&
+        !(H % 256 && static_cast<long>(T) * k <= kFusedDecodeRows)) {
       if (H % 256)
         return fail(MOE_ERR_UNSUPPORTED,
                     "moe_experts_forward: FP4 weights above %d routed rows need H %% 256 == 0",
-                    moe_get_fp4_gemv_rows());
+                    kFusedDecodeRows);
       if (!aligned(w_gate_up, 32) || !aligned(w_down, 32))
         return fail(MOE_ERR_INVALID_ARG,
                     "moe_experts_forward: FP4 weights must be 32-byte aligned (packed TMA loads)");
@@ -427,8 +428,10 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
 
   const int sms = num_sms();
   cudaError_t e;
-  const bool mx = (fp8 && sfmt == MOE_SCALE_UE8M0 && moe_get_block_scaled_mma()) ||
-                  (fp4 && n > moe_get_fp4_gemv_rows());
+  // FP4: the block-scaled GEMMs above the GEMV threshold, except where their
+  // 256-wide down tiles do not divide H and the GEMVs can take the batch
+  const bool fp4_gemm = fp4 && n > moe_get_fp4_gemv_rows() && !(H % 256 && n <= kFusedDecodeRows);
+  const bool mx = (fp8 && sfmt == MOE_SCALE_UE8M0 && moe_get_block_scaled_mma()) || fp4_gemm;
   if (mx) {
     // FP8 (UE8M0) or FP4 experts on the tensor core's block scaling:
     // dispatch, gather + e4m3 quantisation of the rows in 1x128 (FP8) or 1x32

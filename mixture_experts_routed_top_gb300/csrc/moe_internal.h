@@ -210,6 +210,7 @@ struct DecodeArgs {
 constexpr int kDecodeRowsDefault = 16;    // T*k at or below: decode path (measured crossover)
 constexpr int kDecodeRowsMax = 2048;      // the decode path's workspace is sized up to this
 constexpr int kFusedDecodeRows = 64;      // T*k at or below: two fused decode kernels
+constexpr int kFp4GemvRowsDefault = 0;    // FP4: block-scaled GEMMs at every size (measured faster)
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int E, int k,
                                   const DispatchBufs& d, cudaStream_t s);
 cudaError_t launch_decode_gate_up(const DecodeArgs& a, cudaStream_t s);

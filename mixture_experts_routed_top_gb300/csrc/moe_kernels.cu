@@ -115,13 +115,15 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
   }
   if (bad) atomicOr(err, ERR_BAD_INDEX);
   __syncthreads();
+  // expert-major: the scan reads each expert's chunk counts contiguously
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    blk_counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
+    blk_counts[static_cast<long>(e) * gridDim.x + blockIdx.x] = hist[e];
 }
 
-// Per-chunk counts -> per-chunk write bases.  Warp w handles experts w,
-// w+32, ...: its lanes read that expert's chunk counts 32 chunks at a time
-// (independent loads in flight) and a warp scan carries the running base.
+// Per-chunk counts -> per-chunk write bases.  Counts are stored expert-major
+// (blk_counts[e * nchunks + chunk]).  Warp w handles experts w, w+32, ...:
+// its lanes read that expert's chunk counts 32 contiguous chunks at a time
+// and a warp scan carries the running base.
 // Then one block-wide scan over experts gives counts, offsets, the m-tile
 // prefix and the touched list, and the bases are shifted by the offsets.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks, int* blk_counts,
@@ -132,22 +134,40 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks,
   __shared__ int s_warp[33];
   __shared__ int s_tot[kMaxE];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = warp; e < E; e += 32) {
-    int carry = 0;
-    for (int b0 = 0; b0 < nchunks; b0 += 32) {
-      const int b = b0 + lane;
-      const long i = static_cast<long>(b) * E + e;
-      const int v = b < nchunks ? blk_counts[i] : 0;
-      int x = v;
+  // nchunks <= 128: four counts per lane per expert; a batch of 8 experts'
+  // counts is loaded before any of them is scanned and written back
+  constexpr int kQ = 4, kBatch = 8;
+  for (int e0 = warp; e0 < E; e0 += 32 * kBatch) {
+    int v[kBatch][kQ];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
+    for (int j = 0; j < kBatch; ++j) {
+      const int e = e0 + 32 * j;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int b = 32 * q + lane;
+        v[j][q] = (e < E && b < nchunks) ? blk_counts[static_cast<long>(e) * nchunks + b] : 0;
       }
-      if (b < nchunks) blk_counts[i] = carry + x - v;   // exclusive within the expert
-      carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) s_tot[e] = carry;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int e = e0 + 32 * j;
+      if (e >= E) break;
+      int carry = 0;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int b = 32 * q + lane;
+        int x = v[j][q];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (b < nchunks)   // exclusive within the expert
+          blk_counts[static_cast<long>(e) * nchunks + b] = carry + x - v[j][q];
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) s_tot[e] = carry;
+    }
   }
   __syncthreads();
   const int e = threadIdx.x;
@@ -171,9 +191,9 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nchunks,
     touched[0] = tot_h;
   }
   __syncthreads();
-  // shift the per-chunk bases by the expert offsets (coalesced over experts)
+  // shift the per-chunk bases by the expert offsets
   const long total = static_cast<long>(nchunks) * E;
-  for (long i = threadIdx.x; i < total; i += 1024) blk_counts[i] += s_tot[i % E];
+  for (long i = threadIdx.x; i < total; i += 1024) blk_counts[i] += s_tot[i / nchunks];
 }
 
 __global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __restrict__ idx, long n,
@@ -183,7 +203,7 @@ __global__ void __launch_bounds__(32) dispatch_place_kernel(const int32_t* __res
   pdl_wait();
   __shared__ int cursor[kMaxE];
   const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cursor[e] = blk_base[static_cast<long>(blockIdx.x) * E + e];
+  for (int e = lane; e < E; e += 32) cursor[e] = blk_base[static_cast<long>(e) * gridDim.x + blockIdx.x];
   __syncwarp();
   const long base = static_cast<long>(blockIdx.x) * chunk;
   const long end = min(base + chunk, n);
@@ -225,7 +245,9 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
 
 // ============================================================== gather
 // X_perm[r, :] = hidden[sorted_f[r] / k, :] for the rows the dispatch placed
-// (r < offsets[E]); one warp per row, 16-byte vectors.
+// (r < offsets[E]); one warp per row, 16-byte vectors, each lane loading
+// kGatherBatch vectors before storing them.
+constexpr int kGatherBatch = 8;
 __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restrict__ hidden, int H8,
                                                           int k, const int* __restrict__ sorted_f,
                                                           const int* __restrict__ nvalid, int rows,
@@ -238,7 +260,19 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restric
   const long t = __ldg(sorted_f + r) / k;
   const uint4* src = hidden + t * H8;
   uint4* dst = xperm + r * H8;
-  for (int c = lane; c < H8; c += 32) dst[c] = __ldg(src + c);
+  for (int c0 = lane; c0 < H8; c0 += 32 * kGatherBatch) {
+    uint4 v[kGatherBatch];
+#pragma unroll
+    for (int i = 0; i < kGatherBatch; ++i) {
+      const int c = c0 + 32 * i;
+      v[i] = c < H8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kGatherBatch; ++i) {
+      const int c = c0 + 32 * i;
+      if (c < H8) dst[c] = v[i];
+    }
+  }
 }
 
 cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,

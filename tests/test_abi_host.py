@@ -95,14 +95,19 @@ def test_fp4_argument_errors_without_device(L):
     assert f(p, 33, 256, p, p, 8, 2, 128, p16, p, 2, p, p, 2, p, p, 1 << 30, nul) == 1
     assert b"32-byte" in L.moe_last_error()
     assert f(p, 33, 256, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 16, nul) == 5
-    # with the GEMV threshold at 0 even one routed row takes the GEMM path
-    L.moe_set_fp4_gemv_rows(0)
+    # by default even one routed row takes the GEMMs (alignment checked) ...
+    assert L.moe_get_fp4_gemv_rows() == 0
+    assert f(p, 1, 256, p, p, 8, 1, 128, p16, p, 2, p, p, 2, p, p, 1 << 30, nul) == 1
+    # ... unless the GEMV threshold covers the batch (then no alignment rule)
+    L.moe_set_fp4_gemv_rows(64)
     try:
-        assert L.moe_get_fp4_gemv_rows() == 0
-        assert f(p, 1, 128, p, p, 8, 1, 128, p, p, 2, p, p, 2, p, p, 1 << 30, nul) == 2
+        assert L.moe_get_fp4_gemv_rows() == 64
+        assert f(p, 1, 256, p, p, 8, 1, 128, p16, p, 2, p, p, 2, p, p, 16, nul) == 5
     finally:
         L.moe_set_fp4_gemv_rows(-1)
-    assert L.moe_get_fp4_gemv_rows() == 64
+    L.moe_set_fp4_gemv_rows(1000)
+    assert L.moe_get_fp4_gemv_rows() == 64            # clamped
+    L.moe_set_fp4_gemv_rows(-1)
     # T*k = 64 passes those checks and stops at the workspace size
     assert f(p, 32, 128, p, p, 8, 2, 128, p, p, 2, p, p, 2, p, p, 16, nul) == 5
     need = L.moe_workspace_size(32, 128, 128, 8, 2, 2)

@@ -1,10 +1,10 @@
 """Block-scaled tensor-core GEMMs (tcgen05.mma kind::mxf8f6f4 with UE8M0
 scale factors) against the CPU oracle, through the C ABI.
 
-* FP4 (e2m1) experts above 64 routed rows, and below that when the
-  GEMV threshold is set to 0: the mirrored FP4 oracle (same packed weights
-  and 1x32 scales, same dynamic 1x32 e4m3 quantisation of the hidden rows
-  and of h), max|err| / rms(ref) <= 6e-2.
+* FP4 (e2m1) experts, which take these GEMMs at every batch size by
+  default: the mirrored FP4 oracle (same packed weights and 1x32 scales,
+  same dynamic 1x32 e4m3 quantisation of the hidden rows and of h),
+  max|err| / rms(ref) <= 6e-2.
 * FP8 experts with UE8M0 scales on the hardware block scaling and on the
   software promotion kernel: both against the mirrored FP8 oracle.
 * Scales spread over a wide range of powers of two, per 32-wide sub-block
@@ -113,13 +113,19 @@ def test_fp4_block_scaled_parity(moe, shape):
 @pytest.mark.parametrize("shape", [MoEShape(T=1, H=256, I=256, E=16, k=4),
                                    MoEShape(T=8, H=1024, I=512, E=32, k=8)])
 def test_fp4_block_scaled_small_batches(moe, shape):
-    """The GEMMs also take small batches when asked to (threshold 0)."""
-    moe.set_fp4_gemv_rows(0)
-    try:
-        out, ref, launches = _run_fp4(moe, shape)
-    finally:
-        moe.set_fp4_gemv_rows(-1)
+    """Small batches take the GEMMs by default (threshold 0)."""
+    moe.set_fp4_gemv_rows(-1)
+    assert moe.get_fp4_gemv_rows() == 0
+    out, ref, launches = _run_fp4(moe, shape)
     assert launches >= 5
+    assert O.rel_max_err(out, ref) <= TOL
+
+
+def test_fp4_narrow_hidden_small_batch_takes_the_gemvs(moe):
+    """H % 256 != 0: the GEMMs' 256-wide down tiles do not fit, so a batch of
+    at most 64 routed rows runs on the GEMVs (three launches)."""
+    out, ref, launches = _run_fp4(moe, MoEShape(T=4, H=384, I=256, E=8, k=2))
+    assert launches == 3
     assert O.rel_max_err(out, ref) <= TOL
 
 
@@ -150,13 +156,12 @@ def test_fp4_block_scaled_one_expert_takes_all(moe):
 def test_fp4_gemv_and_gemm_paths_agree(moe):
     """The same 64-row FP4 batch through the GEMVs and through the GEMMs."""
     shape = MoEShape(T=16, H=512, I=256, E=8, k=4)
-    moe.set_fp4_gemv_rows(-1)
-    a, ref, la = _run_fp4(moe, shape, seed=7)
-    moe.set_fp4_gemv_rows(0)
+    moe.set_fp4_gemv_rows(64)
     try:
-        b, _, lb = _run_fp4(moe, shape, seed=7)
+        a, ref, la = _run_fp4(moe, shape, seed=7)
     finally:
         moe.set_fp4_gemv_rows(-1)
+    b, _, lb = _run_fp4(moe, shape, seed=7)
     assert la == 3 and lb >= 5
     assert O.rel_max_err(a, ref) <= TOL and O.rel_max_err(b, ref) <= TOL
 

@@ -8,8 +8,9 @@ oracle.
   and of h): max|err| / rms(ref) <= 6e-2, the tolerance used for the FP8
   experts.  Remaining differences come from fp32 accumulation order
   flipping an e4m3 rounding (or a block scale) of h.
-* These shapes run on the small-token GEMVs (T*k <= 64); larger batches run
-  on the block-scaled tensor-core GEMMs (tests/test_gpu_block_scaled.py).
+* These shapes run on the small-token GEMVs (threshold set to 64 routed
+  rows here); by default FP4 runs on the block-scaled tensor-core GEMMs
+  (tests/test_gpu_block_scaled.py).
 """
 import numpy as np
 import pytest
@@ -25,9 +26,14 @@ FP4_TOL = 6e-2
 
 @pytest.fixture(scope="module")
 def moe():
+    """The library with the FP4 GEMV threshold at its maximum (64 routed
+    rows), so these small batches exercise the CUDA-core GEMVs; the default
+    sends them to the block-scaled GEMMs (tests/test_gpu_block_scaled.py)."""
     import mixture_experts_routed_top_gb300 as m
     m.lib()
-    return m
+    m.set_fp4_gemv_rows(64)
+    yield m
+    m.set_fp4_gemv_rows(-1)
 
 
 def test_weight_quantiser_bit_exact(moe):
