@@ -351,6 +351,8 @@ def run_ours(args, rank, world, local_rank):
     moe.set_block_scaled_mma(args.ue8m0_kernel == "block-scaled")
     if args.tile_group is not None:
         moe.set_tile_group(args.tile_group)
+    if args.down_phases is not None:
+        moe.set_down_phases(args.down_phases)
     if args.fp4_gemv_rows is not None:
         moe.set_fp4_gemv_rows(args.fp4_gemv_rows)
     if args.decode_kernels is not None:
@@ -638,6 +640,7 @@ def run_ours(args, rank, world, local_rank):
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
                    "bf16_gemm": args.bf16_gemm, "tile_group": moe.get_tile_group(),
                    "decode_kernels": 1 if moe.get_decode_single() else 2,
+                   "down_phases": moe.get_down_phases(),
                    "activation": args.activation,
                    "scaled_kernels": ("block-scaled tensor-core MMA (kind::mxf8f6f4, UE8M0)"
                                       if mx_path else
@@ -690,6 +693,8 @@ def main():
     ap.add_argument("--ue8m0-kernel", default="block-scaled", choices=["block-scaled", "promotion"],
                     help="FP8 experts with UE8M0 scales: tensor-core block scaling (library "
                          "default) or the software promotion kernel")
+    ap.add_argument("--down-phases", type=int, default=None,
+                    help="output-column slices of the down GEMMs (library default: automatic)")
     ap.add_argument("--fp4-gemv-rows", type=int, default=None,
                     help="FP4 routed rows at or below which the GEMVs run (library default 64)")
     ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],

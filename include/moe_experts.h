@@ -259,8 +259,24 @@ void moe_set_swap_rows(int rows_per_expert);
 int moe_get_swap_rows(void);
 
 /*
- * moe_set_tile_group - tile order of the token-row gate/up GEMM.  Inside an
- * expert the 128-row m-tiles run in groups of m_tiles: every n-tile of one
+ * moe_set_down_phases - tile order of the down GEMMs (bf16 swap-AB and
+ * block-scaled).  Their combine adds every routed row into the fp32
+ * accumulator [T, H] of its token; when that accumulator is larger than L2,
+ * a token's k contributions, made by different experts at different times,
+ * find its lines evicted.  With P phases the output columns are cut into P
+ * slices run one after the other, each over all experts, so only a
+ * [T, H/P] slice is live at a time (the h rows are read once per phase).
+ * phases < 0 (the default): the smallest P that divides the number of
+ * 256-column blocks and brings the slice to at most 64 MB; 0 or 1: one
+ * phase; P > 1: at least P (rounded up to such a divisor).  Process-wide;
+ * moe_get_down_phases returns the setting (-1 = automatic).
+ */
+void moe_set_down_phases(int phases);
+int moe_get_down_phases(void);
+
+/*
+ * moe_set_tile_group - tile order of the token-row gate/up GEMMs (bf16 and
+ * block-scaled).  Inside an expert the 128-row m-tiles run in groups of m_tiles: every n-tile of one
  * group (m fastest), then the next group, so that an expert with many rows
  * re-reads one group's activation tiles per n-tile instead of all of them.
  * 0 puts all of an expert's m-tiles in one group; m_tiles < 0 restores the

@@ -22,7 +22,8 @@ __all__ = [
     "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
     "selftest_wait_timeout", "launch_count", "accumulator", "set_block_scaled_mma",
     "get_block_scaled_mma", "set_fp4_gemv_rows", "get_fp4_gemv_rows", "set_decode_single",
-    "get_decode_single", "set_tile_group", "get_tile_group",
+    "get_decode_single", "set_tile_group", "get_tile_group", "set_down_phases",
+    "get_down_phases",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "W_FP4_E2M1", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0", "ACTIVATIONS",
 ]
@@ -70,6 +71,8 @@ _SIGS = {
     "moe_workspace_accumulator_offset": ([_I, _I, _I, _I, _I, _I], _SZ),
     "moe_set_block_scaled_mma": ([_I], None),
     "moe_get_block_scaled_mma": ([], _I),
+    "moe_set_down_phases": ([_I], None),
+    "moe_get_down_phases": ([], _I),
     "moe_set_tile_group": ([_I], None),
     "moe_get_tile_group": ([], _I),
     "moe_set_decode_single": ([_I], None),
@@ -328,6 +331,16 @@ def set_block_scaled_mma(on: bool):
 
 def get_block_scaled_mma() -> bool:
     return bool(lib().moe_get_block_scaled_mma())
+
+
+def set_down_phases(phases: int):
+    """Output-column slices of the down GEMMs run one after the other (< 0:
+    automatic, the default; 0 or 1: one)."""
+    lib().moe_set_down_phases(int(phases))
+
+
+def get_down_phases() -> int:
+    return int(lib().moe_get_down_phases())
 
 
 def set_tile_group(m_tiles: int):

@@ -93,11 +93,22 @@ struct MxDev {
   const int* sorted_f;
   const float* topk_w;
   int act;
+  int group;                // m-tiles per tile group (0: all of the expert's)
+  int phases;               // n-tile slices run one after the other (>= 1)
 };
 
-__device__ __forceinline__ void decode_tile_mx(int tile, int NT, int E, const int* s_pref, int& e,
-                                               int& m, int& n) {
-  const int v = tile / NT;
+// Tile -> (expert e, m-tile m, n-tile n).  The n-tiles are cut into
+// `phases` equal slices run one after the other (the down GEMM's combine
+// then touches a T x H/phases slice of the fp32 accumulator at a time).
+// Inside a slice and an expert the m-tiles run in groups of `group` (0:
+// all): a group's tiles for every n-tile of the slice, m fastest.
+__device__ __forceinline__ void decode_tile_mx(int tile, int NT, int E, const int* s_pref,
+                                               int group, int phases, int& e, int& m, int& n) {
+  const int ntp = NT / phases;
+  const int per_phase = s_pref[E] * ntp;
+  const int ph = tile / per_phase;
+  tile -= ph * per_phase;
+  const int v = tile / ntp;
   int lo = 0, hi = E;
   while (lo < hi) {  // largest e with s_pref[e] <= v
     const int mid = (lo + hi + 1) >> 1;
@@ -106,9 +117,13 @@ __device__ __forceinline__ void decode_tile_mx(int tile, int NT, int E, const in
   }
   e = lo;
   const int mt = s_pref[e + 1] - s_pref[e];
-  const int local = tile - s_pref[e] * NT;
-  n = local / mt;
-  m = local - n * mt;
+  const int local = tile - s_pref[e] * ntp;
+  const int G = (group > 0 && group < mt) ? group : mt;
+  const int g = local / (G * ntp);
+  const int gg = min(G, mt - g * G);
+  const int r = local - g * G * ntp;
+  n = ph * ntp + r / gg;
+  m = g * G + (r - (r / gg) * gg);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -209,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto place = [&](Cursor& c) {
       if (c.tile >= total) return;
       int e, m, n;
-      decode_tile_mx(c.tile, NT, E, s_pref, e, m, n);
+      decode_tile_mx(c.tile, NT, E, s_pref, p.group, p.phases, e, m, n);
       c.arow = s_off[e] + m * BM;
       c.brow0 = (EPI == EPI_SWIGLU_Q) ? e * Nw + n * 128 : e * Nw + n * BN;
       c.brow1 = (EPI == EPI_SWIGLU_Q) ? c.brow0 + p.I : c.brow0 + 128;
@@ -382,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       int e, m, n;
-      decode_tile_mx(tile, NT, E, s_pref, e, m, n);
+      decode_tile_mx(tile, NT, E, s_pref, p.group, p.phases, e, m, n);
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_bounded<true>(smem_u32(tfull), it & 1, s_abort, p.err,
@@ -575,6 +590,8 @@ cudaError_t launch_mx_impl(const GroupedGemmMxArgs& a, cudaStream_t s) {
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
   p.act = a.act;
+  p.group = a.tile_group;
+  p.phases = a.phases > 0 ? a.phases : 1;
   launch_pdl(kern, a.num_sms, kThreads, LM::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

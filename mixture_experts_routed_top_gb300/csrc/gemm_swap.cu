@@ -66,14 +66,25 @@ struct GemmDev {
   const int* sorted_f;
   const float* topk_w;
   int act;               // moe_activation of the gate/up epilogue
+  int phases;            // feature-block slices run one after the other (>= 1)
 };
 
 struct Tile {
   int e, fb, t0, size;
 };
 
+// Tile -> (expert, feature block, token tile).  With phases > 1 the feature
+// blocks are cut into `phases` equal slices that run one after the other
+// (every expert's tiles of slice 0, then of slice 1, ...), so the down GEMM's
+// combine only touches a T x H/phases slice of the fp32 accumulator at a
+// time; inside a slice the order is expert, feature block, token tile.
 __device__ __forceinline__ Tile decode_tile(int tile, int NFT, int E, const int* s_off,
-                                            const int* s_pref) {
+                                            const int* s_pref, int phases) {
+  const int nfp = NFT / phases;
+  const int per_phase = s_pref[E] * nfp;
+  const int ph = tile / per_phase;
+  tile -= ph * per_phase;
+  NFT = nfp;
   const int v = tile / NFT;
   int lo = 0, hi = E;
   while (lo < hi) {  // largest e with s_pref[e] <= v
@@ -85,10 +96,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NFT, int E, const int*
   t.e = lo;
   const int ntt = s_pref[lo + 1] - s_pref[lo];
   const int local = tile - s_pref[lo] * NFT;
-  t.fb = local / ntt;
-  const int j = local - t.fb * ntt;
+  t.fb = ph * nfp + local / ntt;
+  const int j = local - (local / ntt) * ntt;
   const int M = s_off[lo + 1] - s_off[lo];
-  const int b = (j * M) / ntt, en = ((j + 1) * M) / ntt;  // sizes differ by <= 1
+  const int b = static_cast<int>(static_cast<long>(j) * M / ntt);      // sizes differ by <= 1
+  const int en = static_cast<int>(static_cast<long>(j + 1) * M / ntt);
   t.t0 = s_off[lo] + b;
   t.size = en - b;
   return t;
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, NFT, E, s_off, s_pref);
+        const Tile t = decode_tile(tile, NFT, E, s_off, s_pref, p.phases);
         const int nbox = (t.size + 63) >> 6;
         const uint32_t tx = NA * A_BOX + nbox * B_BOX;
         int wrow0, wrow1;
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
-        const Tile t = decode_tile(tile, NFT, E, s_off, s_pref);
+        const Tile t = decode_tile(tile, NFT, E, s_off, s_pref, p.phases);
         const int N = (t.size + 15) & ~15;  // <= kMaxN
         const uint32_t idesc = idesc_bf16_f32(128, N);
         const int acc = it & 1;
@@ -254,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const Tile t = decode_tile(tile, NFT, E, s_off, s_pref);
+      const Tile t = decode_tile(tile, NFT, E, s_off, s_pref, p.phases);
       const int acc = it & 1;
       int ok = 1;
       if (lane == 0)
@@ -343,6 +355,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
   p.act = a.act;
+  p.phases = a.phases > 0 ? a.phases : 1;
   launch_pdl(kern, a.num_sms, kThreads, SMEM_BYTES, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

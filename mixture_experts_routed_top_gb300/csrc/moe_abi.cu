@@ -67,6 +67,7 @@ std::atomic<int> g_block_scaled_mma{1};   // UE8M0 FP8 experts on the tensor cor
 std::atomic<int> g_fp4_gemv_rows{-1};     // FP4: CUDA-core GEMVs up to this many routed rows
 std::atomic<int> g_decode_single{0};      // small decode batches as one cooperative launch
 std::atomic<int> g_tile_group{-1};        // token-row gate/up GEMM: m-tiles per tile group
+std::atomic<int> g_down_phases{-1};       // down GEMMs: accumulator slices (< 0: automatic)
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -251,6 +252,9 @@ int moe_get_swap_rows(void) {
   const int r = g_swap_rows.load(std::memory_order_relaxed);
   return r < 0 ? kSwapRowsDefault : r;
 }
+
+void moe_set_down_phases(int phases) { g_down_phases = phases < 0 ? -1 : phases; }
+int moe_get_down_phases(void) { return g_down_phases.load(std::memory_order_relaxed); }
 
 void moe_set_tile_group(int m_tiles) { g_tile_group = m_tiles < 0 ? -1 : m_tiles; }
 int moe_get_tile_group(void) {
@@ -484,6 +488,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     g.topk_w = topk_w;
     g.act = static_cast<int>(act);
     const long mtiles_max = n / kBM + E;
+    g.tile_group = moe_get_tile_group();
     {
       StageScope sc(s, MOE_STAGE_GEMM1);
       g.tm_a = &tm_x;
@@ -502,6 +507,8 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       g.a_sf = hs;
       g.w_sf = static_cast<const uint8_t*>(scale_down);
       g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / 256)));
+      g.tile_group = 0;
+      g.phases = down_phases(T, H, H / 256, g_down_phases.load(std::memory_order_relaxed));
       if ((e = launch_gemm2_mx(g, fp4, s)) != cudaSuccess) return cuda_fail(e, "gemm2_mx");
     }
     {
@@ -751,6 +758,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     g.K = I;
     const int nf = (H % 256 == 0) ? 256 : 128;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / nf)));
+    g.phases = down_phases(T, H, H / nf, g_down_phases.load(std::memory_order_relaxed));
     e = swap2 ? launch_gemm2_bf16_swap(g, s) : launch_gemm2_bf16_rows(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm2");
   }

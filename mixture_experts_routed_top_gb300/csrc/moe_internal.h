@@ -129,6 +129,7 @@ struct GroupedGemmArgs {
   int num_sms;
   int act;                   // moe_activation of the gate/up epilogue
   int tile_group = 0;        // token-row kernel: m-tiles per tile group (0: all)
+  int phases = 1;            // swap-AB kernel: feature-block slices run in turn
 };
 cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
@@ -137,6 +138,20 @@ cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
 constexpr int kTileGroupDefault = 4;   // token-row gate/up: m-tiles per tile group (measured)
+// Down GEMMs: the fp32 accumulator slice [T, H/phases] that one phase
+// updates is kept at or below this many bytes (automatic phase count).
+constexpr long kDownPhaseBytes = 64L << 20;
+// Number of slices (a divisor of nblocks) that brings T*H*4/slices to at
+// most kDownPhaseBytes; `forced` > 0 asks for that many (rounded up to a
+// divisor).
+inline int down_phases(long T, long H, int nblocks, int forced) {
+  const long acc = T * H * 4;
+  for (int d = 1; d <= nblocks; ++d) {
+    if (nblocks % d) continue;
+    if (forced > 0 ? d >= forced : acc / d <= kDownPhaseBytes) return d;
+  }
+  return nblocks;
+}
 
 // FP8 e4m3 block-scaled grouped GEMMs (scales applied per 128-wide K-block).
 struct GroupedGemmFp8Args {
@@ -182,6 +197,8 @@ struct GroupedGemmMxArgs {
   const float* topk_w;
   int num_sms;
   int act;
+  int tile_group = 0;        // m-tiles per tile group (0: all)
+  int phases = 1;            // n-tile slices run in turn
 };
 cudaError_t launch_gemm1_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
 cudaError_t launch_gemm2_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);

@@ -166,6 +166,24 @@ def test_fp4_gemv_and_gemm_paths_agree(moe):
     assert O.rel_max_err(a, ref) <= TOL and O.rel_max_err(b, ref) <= TOL
 
 
+@pytest.mark.parametrize("fmt", ["fp4", "fp8"])
+def test_block_scaled_down_gemm_phases_and_groups(moe, fmt):
+    """Down GEMM output columns in four slices and gate/up m-tiles in groups
+    of two (an expert with 5 m-tiles): every tile still runs exactly once."""
+    shape = MoEShape(T=700, H=1024, I=256, E=2, k=2)
+    moe.set_down_phases(4)
+    moe.set_tile_group(2)
+    try:
+        if fmt == "fp4":
+            out, ref, _ = _run_fp4(moe, shape)
+        else:
+            out, ref = _run_fp8(moe, shape)
+    finally:
+        moe.set_down_phases(-1)
+        moe.set_tile_group(-1)
+    assert O.rel_max_err(out, ref) <= TOL
+
+
 FP8_SHAPES = [
     MoEShape(T=64, H=256, I=256, E=8, k=2),
     MoEShape(T=300, H=512, I=384, E=6, k=3),

@@ -145,6 +145,19 @@ def test_forward_bf16_parity(moe, shape, path):
     assert np.all(np.isfinite(out))
 
 
+@pytest.mark.parametrize("phases", [2, 4])
+def test_forward_bf16_down_gemm_phases(moe, phases):
+    """The down GEMM's output columns in 2 or 4 slices run one after the
+    other (the order used when the fp32 accumulator exceeds L2): every tile
+    still runs exactly once."""
+    moe.set_down_phases(phases)
+    try:
+        out, ref = _forward_case(moe, MoEShape(T=300, H=1024, I=384, E=6, k=3))
+    finally:
+        moe.set_down_phases(-1)
+    assert O.rel_max_err(out, ref) <= BF16_TOL
+
+
 @pytest.mark.parametrize("path", ["rows", "swap"], indirect=True)
 def test_forward_bf16_parity_qwen_shape_520_tokens(moe, path):
     out, ref = _forward_case(moe, MoEShape(T=520, H=2048, I=1408, E=60, k=4))
