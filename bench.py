@@ -353,6 +353,8 @@ def run_ours(args, rank, world, local_rank):
         moe.set_tile_group(args.tile_group)
     if args.down_phases is not None:
         moe.set_down_phases(args.down_phases)
+    if args.pair_gemm is not None:
+        moe.set_pair_gemm(args.pair_gemm)
     if args.fp4_gemv_rows is not None:
         moe.set_fp4_gemv_rows(args.fp4_gemv_rows)
     if args.decode_kernels is not None:
@@ -641,6 +643,7 @@ def run_ours(args, rank, world, local_rank):
                    "bf16_gemm": args.bf16_gemm, "tile_group": moe.get_tile_group(),
                    "decode_kernels": 1 if moe.get_decode_single() else 2,
                    "down_phases": moe.get_down_phases(),
+                   "pair_gemm": moe.get_pair_gemm(),
                    "activation": args.activation,
                    "scaled_kernels": ("block-scaled tensor-core MMA (kind::mxf8f6f4, UE8M0)"
                                       if mx_path else
@@ -699,6 +702,9 @@ def main():
                     help="FP4 routed rows at or below which the GEMVs run (library default 64)")
     ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],
                     help="small bf16 decode batches as one cooperative kernel or two kernels "
+                         "(library default)")
+    ap.add_argument("--pair-gemm", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="bf16 grouped GEMMs on CTA pairs: bit 0 gate/up, bit 1 down "
                          "(library default)")
     ap.add_argument("--tile-group", type=int, default=None,
                     help="m-tiles per tile group of the token-row gate/up GEMM (library default)")

@@ -267,12 +267,25 @@ int moe_get_swap_rows(void);
  * slices run one after the other, each over all experts, so only a
  * [T, H/P] slice is live at a time (the h rows are read once per phase).
  * phases < 0 (the default): the smallest P that divides the number of
- * 256-column blocks and brings the slice to at most 64 MB; 0 or 1: one
+ * 256-column blocks and brings the slice to at most 40 MB; 0 or 1: one
  * phase; P > 1: at least P (rounded up to such a divisor).  Process-wide;
  * moe_get_down_phases returns the setting (-1 = automatic).
  */
 void moe_set_down_phases(int phases);
 int moe_get_down_phases(void);
+
+/*
+ * moe_set_pair_gemm - bf16 grouped GEMMs (forwards above the decode
+ * threshold) on CTA pairs: tcgen05.mma.cta_group::2, 256 weight rows (128
+ * per SM) against up to 256 of an expert's tokens.  mask bit 0: the gate/up
+ * GEMM, bit 1: the down GEMM (only where H % 256 == 0; else the one-CTA
+ * kernel runs); mask < 0 restores the default: gate/up on pairs where
+ * H >= 4096 (measured faster at DeepSeek-V3 width, slower at H = 2048), the
+ * down GEMM on one-CTA kernels (measured faster at every size).
+ * Process-wide; moe_get_pair_gemm returns the mask set (-1 = the default).
+ */
+void moe_set_pair_gemm(int mask);
+int moe_get_pair_gemm(void);
 
 /*
  * moe_set_tile_group - tile order of the token-row gate/up GEMMs (bf16 and

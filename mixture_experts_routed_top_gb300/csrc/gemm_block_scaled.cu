@@ -219,13 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // factors of its iteration into one of kSfAhead register slots, so no
     // stage waits for a global-memory round trip of its scale factors.
     struct Cursor {
-      int tile, kb, arow, brow0, brow1;
+      int tile, kb, arow, brow0, brow1, e, n;
     };
     auto place = [&](Cursor& c) {
       if (c.tile >= total) return;
       int e, m, n;
       decode_tile_mx(c.tile, NT, E, s_pref, p.group, p.phases, e, m, n);
       c.arow = s_off[e] + m * BM;
+      c.e = e;
+      c.n = n;
       c.brow0 = (EPI == EPI_SWIGLU_Q) ? e * Nw + n * 128 : e * Nw + n * BN;
       c.brow1 = (EPI == EPI_SWIGLU_Q) ? c.brow0 + p.I : c.brow0 + 128;
     };
@@ -300,8 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_dst = smem_u32(sA + stage * LM::A_BYTES);
         const uint32_t b_dst = smem_u32(sB + stage * LM::B_BYTES);
         tma_load_2d(&tm_a, fb, a_dst, ld.kb * BK, ld.arow);
-        tma_load_2d(&tm_b, fb, b_dst, ld.kb * BK, ld.brow0);
-        tma_load_2d(&tm_b, fb, b_dst + LM::B_BYTES / 2, ld.kb * BK, ld.brow1);
+        if (EPI == EPI_SWIGLU_Q)  // 128 gate rows, then their up rows: one 3-D box
+          tma_load_3d(&tm_b, fb, b_dst, ld.kb * BK, ld.n * 128, 2 * ld.e);
+        else                      // 256 rows of W_down[e]: one box
+          tma_load_2d(&tm_b, fb, b_dst, ld.kb * BK, ld.brow0);
       }
       // this stage's scale factors (loaded kSfAhead iterations ago) into
       // shared memory, then the slot takes those of iteration + kSfAhead

@@ -46,7 +46,6 @@ constexpr int kGroupCols = 256 / kEpiGroups;  // partial-sum columns per warpgro
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kBufCols = 256;
-constexpr int kBoxBytes = 128 * 128;
 
 enum { EPI_SWIGLU_Q = 0, EPI_COMBINE = 1 };
 
@@ -181,7 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int e, m, n;
         decode_tile8(tile, NT, E, s_pref, e, m, n);
         const int arow = s_off[e] + m * BM;
-        const int brow = (EPI == EPI_SWIGLU_Q) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
+        // gate/up: feature n*128 in the [2E, I, H] view; down: the first of
+        // the tile's 256 rows of W_down[e]
+        const int brow = (EPI == EPI_SWIGLU_Q) ? n * 128 : e * p.H + n * BN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
@@ -193,13 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = smem_u32(sA + stage * L8::A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * L8::B_BYTES);
           tma_load_2d(&tm_a, fb, a_dst, kb * BK, arow);
-          if (EPI == EPI_SWIGLU_Q) {
+          if (EPI == EPI_SWIGLU_Q)  // 128 gate rows, then their up rows: one 3-D box
+            tma_load_3d(&tm_b, fb, b_dst, kb * BK, brow, 2 * e);
+          else                      // 256 rows of W_down[e]: one box
             tma_load_2d(&tm_b, fb, b_dst, kb * BK, brow);
-            tma_load_2d(&tm_b, fb, b_dst + kBoxBytes, kb * BK, brow + p.I);
-          } else {
-            tma_load_2d(&tm_b, fb, b_dst, kb * BK, brow);
-            tma_load_2d(&tm_b, fb, b_dst + kBoxBytes, kb * BK, brow + 128);
-          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (ph << stage);
           if (++stage == kStages) {

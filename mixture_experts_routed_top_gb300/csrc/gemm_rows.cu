@@ -170,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int e, m, n;
         decode_tile(tile, NT, E, s_pref, p.group, e, m, n);
         const int arow = s_off[e] + m * BM;
-        const int brow = (EPI == EPI_SWIGLU) ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
+        // gate/up: feature n*128 in the [2E, I, H] view of the weights; down:
+        // the first W_down row of the n-tile
+        const int brow = (EPI == EPI_SWIGLU) ? n * 128 : e * p.H + n * BN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
@@ -182,9 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = smem_u32(sA + stage * L::A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * L::B_BYTES);
           tma_load_2d(&tm_a, fb, a_dst, kb * BK, arow);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(&tm_b, fb, b_dst, kb * BK, brow);
-            tma_load_2d(&tm_b, fb, b_dst + kBoxBytes, kb * BK, brow + p.I);
+          if (EPI == EPI_SWIGLU) {  // 128 gate rows, then their up rows: one 3-D box
+            tma_load_3d(&tm_b, fb, b_dst, kb * BK, brow, 2 * e);
           } else {
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)

@@ -169,21 +169,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t ph = 0, issued = 0, last_par = 0;
       bool ok = true;
-      auto weight_rows = [&](const Tile& t, int& w0, int& w1) {
-        if (EPI == EPI_SWIGLU) {
-          w0 = t.e * 2 * p.I + t.fb * 128;
-          w1 = w0 + p.I;
-        } else {
-          w0 = t.e * p.H + t.fb * 128 * NA;
-          w1 = w0 + 128;
-        }
+      // gate/up: feature fb*128 in the [2E, I, H] view of the weights (one
+      // 3-D box: 128 gate rows, then their up rows); down: the first of the
+      // tile's 128*NA rows of W_down[e] (one box of 128*NA rows)
+      auto weight_row = [&](const Tile& t) {
+        return EPI == EPI_SWIGLU ? t.fb * 128 : t.e * p.H + t.fb * 128 * NA;
       };
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const Tile t = decode_tile(tile, NFT, E, s_off, s_pref, p.phases);
         const int nbox = (t.size + 63) >> 6;
         const uint32_t tx = NA * A_BOX + nbox * B_BOX;
-        int wrow0, wrow1;
-        weight_rows(t, wrow0, wrow1);
+        const int wrow = weight_row(t);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded<true>(smem_u32(&empty[stage]), ph ^ 1u, s_abort, p.err,
                                  ERR_TIMEOUT_PRODUCER)) {
@@ -194,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(fb, tx);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          tma_load_2d(&tm_w, fb, a_dst, kb * BK, wrow0);
-          if (NA == 2) tma_load_2d(&tm_w, fb, a_dst + A_BOX, kb * BK, wrow1);
+          if (EPI == EPI_SWIGLU) tma_load_3d(&tm_w, fb, a_dst, kb * BK, wrow, 2 * t.e);
+          else tma_load_2d(&tm_w, fb, a_dst, kb * BK, wrow);
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(&tm_x, fb, b_dst + b * B_BOX, kb * BK, t.t0 + 64 * b);
           issued |= 1u << stage;
@@ -363,7 +359,8 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// tm_a: weights (box 128 rows), tm_b: activations (box 64 rows),
+// tm_a: weights (gate/up: the [2E, I, H] view with boxes {64, 128, 2};
+// down: boxes of 128 * NA rows), tm_b: activations (box 64 rows),
 // tile_pref: prefix of ceil(M_e / 128).
 cudaError_t launch_gemm1_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_impl<EPI_SWIGLU, 2>(a, s);

@@ -68,6 +68,7 @@ std::atomic<int> g_fp4_gemv_rows{-1};     // FP4: CUDA-core GEMVs up to this man
 std::atomic<int> g_decode_single{0};      // small decode batches as one cooperative launch
 std::atomic<int> g_tile_group{-1};        // token-row gate/up GEMM: m-tiles per tile group
 std::atomic<int> g_down_phases{-1};       // down GEMMs: accumulator slices (< 0: automatic)
+std::atomic<int> g_pair_gemm{-1};         // bf16 grouped GEMMs on CTA pairs (bit mask, < 0: default)
 
 // ----------------------------------------------------------- workspace map
 struct WsLayout {
@@ -155,16 +156,39 @@ moe_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
   return MOE_OK;
 }
 
+// Gate/up weights [E, 2I, K] viewed as 3-D [2E, I, K] (plane 2e = the gate
+// rows of expert e, plane 2e+1 its up rows): a box {row_bytes / esize
+// elements, box_rows, 2} brings box_rows gate rows and then the matching up
+// rows, swizzled at 128 bytes.  For packed e2m1 (dt 16U4_ALIGN16B) K counts
+// elements and a row holds K/2 bytes.
+moe_status make_map_gate_up(CUtensorMap* m, const void* base, CUtensorMapDataType dt,
+                            uint64_t K, uint64_t I, uint64_t E, uint32_t box_rows,
+                            uint32_t box_elems, uint64_t row_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {K, I, 2 * E};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * I};
+  cuuint32_t box[3] = {box_elems, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (gate/up view) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 // 2-D packed e2m1 matrix [rows, k_elems] (two codes per byte, row stride
-// k_elems/2 bytes), box 128 elements x 128 rows, expanded by TMA into the
+// k_elems/2 bytes), box 128 elements x box_rows rows, expanded by TMA into the
 // one-byte-per-element-slot shared-memory form (16 codes in 8 bytes, 8 bytes
 // of padding) and swizzled at 128 bytes.
-moe_status make_map_e2m1(CUtensorMap* m, const void* base, uint64_t k_elems, uint64_t rows) {
+moe_status make_map_e2m1(CUtensorMap* m, const void* base, uint64_t k_elems, uint64_t rows,
+                         uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {k_elems, rows};
   cuuint64_t strides[1] = {k_elems / 2};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -252,6 +276,9 @@ int moe_get_swap_rows(void) {
   const int r = g_swap_rows.load(std::memory_order_relaxed);
   return r < 0 ? kSwapRowsDefault : r;
 }
+
+void moe_set_pair_gemm(int mask) { g_pair_gemm = mask < 0 ? -1 : (mask & 3); }
+int moe_get_pair_gemm(void) { return g_pair_gemm.load(std::memory_order_relaxed); }
 
 void moe_set_down_phases(int phases) { g_down_phases = phases < 0 ? -1 : phases; }
 int moe_get_down_phases(void) { return g_down_phases.load(std::memory_order_relaxed); }
@@ -448,17 +475,20 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     moe_status st;
     if ((st = make_map(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, n)) != MOE_OK) return st;
     if ((st = make_map(&tm_h, hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, n)) != MOE_OK) return st;
+    // gate/up weights: the [2E, I, H] view, one box = 128 gate rows and
+    // their up rows; down weights: 256-row boxes
     if (fp4) {
-      if ((st = make_map_e2m1(&tm_wgu, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+      if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, H, I,
+                                 E, 128, 128, static_cast<uint64_t>(H) / 2)) != MOE_OK)
         return st;
-      if ((st = make_map_e2m1(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H)) != MOE_OK)
+      if ((st = make_map_e2m1(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, 256)) != MOE_OK)
         return st;
     } else {
-      if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H,
-                         static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+      if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, H, I, E, 128,
+                                 128, H)) != MOE_OK)
         return st;
       if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I,
-                         static_cast<uint64_t>(E) * H)) != MOE_OK)
+                         static_cast<uint64_t>(E) * H, 256)) != MOE_OK)
         return st;
     }
     {
@@ -627,12 +657,12 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
     moe_status st;
     if ((st = make_map(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, n)) != MOE_OK) return st;
-    if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H,
-                       static_cast<uint64_t>(E) * 2 * I)) != MOE_OK)
+    if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_UINT8, H, I, E, 128,
+                               128, H)) != MOE_OK)
       return st;
     if ((st = make_map(&tm_h, hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, n)) != MOE_OK) return st;
     if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I,
-                       static_cast<uint64_t>(E) * H)) != MOE_OK)
+                       static_cast<uint64_t>(E) * H, 256)) != MOE_OK)
       return st;
     {
       StageScope sc(s, MOE_STAGE_DISPATCH);
@@ -697,22 +727,35 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   const int swap_rows = moe_get_swap_rows();
   const bool swap1 = n <= static_cast<long>(swap_rows) * E;
   const bool swap2 = g_swap_rows.load(std::memory_order_relaxed) >= 0 ? swap1 : true;
+  // CTA-pair kernels (either GEMM, by the process-wide mask)
+  const int pair_set = moe_get_pair_gemm();
+  const int pair = pair_set < 0 ? pair_gemm_default(H) : pair_set;
+  const bool pair1 = pair & 1;
+  const bool pair2 = (pair & 2) && H % 256 == 0;
   // swap-AB kernel: 128-byte rows, token boxes of 64 rows; token-row
-  // kernel: rows of kRowsBK bf16, 128-row boxes for both operands
+  // kernel: rows of kRowsBK bf16, 128-row boxes for both operands; pair
+  // kernel: 128-byte rows, 128-row token boxes, weight boxes of 64 rows
+  // (gate/up) or 128 (down)
   const uint32_t rb = kRowsBK * 2;
+  // gate/up weights: the [2E, I, H] view, one box = box rows of gate and the
+  // matching up rows; down weights: 128-row boxes (swap-AB: 128 per M=128
+  // MMA of the tile, so 256 where H % 256 == 0)
+  const uint32_t xr1 = swap1 && !pair1 ? 64 : 128, wr1 = pair1 ? 64 : 128;
+  const uint32_t xb1 = (pair1 || swap1) ? 128 : rb;
+  const uint32_t xr2 = swap2 && !pair2 ? 64 : 128;
+  const uint32_t wr2 = swap2 && !pair2 && H % 256 == 0 ? 256 : 128;
+  const uint32_t xb2 = (pair2 || swap2) ? 128 : rb;
   CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
   moe_status st;
-  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, swap1 ? 64 : 128,
-                     swap1 ? 128 : rb)) != MOE_OK)
+  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, xr1, xb1)) != MOE_OK)
     return st;
-  if ((st = make_map(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
-                     static_cast<uint64_t>(E) * 2 * I, 128, swap1 ? 128 : rb)) != MOE_OK)
+  if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, I, E, wr1,
+                             xb1 / 2, static_cast<uint64_t>(H) * 2)) != MOE_OK)
     return st;
-  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, swap2 ? 64 : 128,
-                     swap2 ? 128 : rb)) != MOE_OK)
+  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, xr2, xb2)) != MOE_OK)
     return st;
   if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
-                     static_cast<uint64_t>(E) * H, 128, swap2 ? 128 : rb)) != MOE_OK)
+                     static_cast<uint64_t>(E) * H, wr2, xb2)) != MOE_OK)
     return st;
 
   {
@@ -743,23 +786,25 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   const long mtiles_max = n / kBM + E;
   {
     StageScope sc(s, MOE_STAGE_GEMM1);
-    g.tm_a = swap1 ? &tm_wgu : &tm_x;
-    g.tm_b = swap1 ? &tm_x : &tm_wgu;
+    g.tm_a = (swap1 || pair1) ? &tm_wgu : &tm_x;
+    g.tm_b = (swap1 || pair1) ? &tm_x : &tm_wgu;
     g.K = H;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
     g.tile_group = moe_get_tile_group();
-    e = swap1 ? launch_gemm1_bf16_swap(g, s) : launch_gemm1_bf16_rows(g, s);
+    e = pair1 ? launch_gemm1_bf16_pair(g, n, s)
+              : swap1 ? launch_gemm1_bf16_swap(g, s) : launch_gemm1_bf16_rows(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm1");
   }
   {
     StageScope sc(s, MOE_STAGE_GEMM2);
-    g.tm_a = swap2 ? &tm_wd : &tm_h;
-    g.tm_b = swap2 ? &tm_h : &tm_wd;
+    g.tm_a = (swap2 || pair2) ? &tm_wd : &tm_h;
+    g.tm_b = (swap2 || pair2) ? &tm_h : &tm_wd;
     g.K = I;
     const int nf = (H % 256 == 0) ? 256 : 128;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / nf)));
     g.phases = down_phases(T, H, H / nf, g_down_phases.load(std::memory_order_relaxed));
-    e = swap2 ? launch_gemm2_bf16_swap(g, s) : launch_gemm2_bf16_rows(g, s);
+    e = pair2 ? launch_gemm2_bf16_pair(g, n, s)
+              : swap2 ? launch_gemm2_bf16_swap(g, s) : launch_gemm2_bf16_rows(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm2");
   }
   {

@@ -135,12 +135,25 @@ cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm1_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+// The same GEMMs on CTA pairs (gemm_pair.cu: tcgen05.mma.cta_group::2,
+// M = 256 weight rows, tokens as N <= 256; tm_a = weights, tm_b =
+// activations with 64- (gate/up) or 128-row (down) weight boxes and 128-row
+// token boxes; the tile prefix is built in the
+// kernel; down needs H % 256 == 0).  n_rows = routed rows (T*k).
+cudaError_t launch_gemm1_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaStream_t s);
+cudaError_t launch_gemm2_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaStream_t s);
+// Default CTA-pair use (bit 0: gate/up, bit 1: down): gate/up on pairs for
+// H >= kPairGateUpMinH, measured faster there (DeepSeek-V3 width) and
+// slower at H = 2048 (Qwen width, whose ~140-token tiles leave the pair
+// bound by L2 reads); the down GEMM measured slower on pairs everywhere.
+constexpr int kPairGateUpMinH = 4096;
+inline int pair_gemm_default(int H) { return H >= kPairGateUpMinH ? 1 : 0; }
 constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
 constexpr int kTileGroupDefault = 4;   // token-row gate/up: m-tiles per tile group (measured)
 // Down GEMMs: the fp32 accumulator slice [T, H/phases] that one phase
 // updates is kept at or below this many bytes (automatic phase count).
-constexpr long kDownPhaseBytes = 64L << 20;
+constexpr long kDownPhaseBytes = 40L << 20;   // measured: 7 slices at DeepSeek-V3 T=8192, 14 at T=16384
 // Number of slices (a divisor of nblocks) that brings T*H*4/slices to at
 // most kDownPhaseBytes; `forced` > 0 asks for that many (rounded up to a
 // divisor).

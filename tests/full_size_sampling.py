@@ -6,8 +6,10 @@ oracle runs on a sample.  The sample is chosen to reach every tile the
 grouped GEMMs cut the expert-sorted rows into:
 
 * for the expert with the most rows, the first and the last row of every
-  128-row tile of the token-row GEMM and of every near-equal token tile of
-  the swap-AB GEMM (so both sides of every tile boundary, and the last tile);
+  128-row tile of the token-row GEMM, of every near-equal token tile of the
+  swap-AB GEMM (at most 128 rows) and of every near-equal token tile of the
+  CTA-pair GEMM (at most 256 rows), so both sides of every tile boundary,
+  and the last tile;
 * for every other touched expert, its first and last row.
 
 A row stands for its token.  With ``cheap`` (a set of experts), only tokens
@@ -32,14 +34,21 @@ import torch
 import oracle as O
 
 TILE_ROWS = 128
+PAIR_TILE_ROWS = 256
 
 
 def _segments(o, M):
     """Row ranges of the tiles of one expert (rows [o, o+M))."""
     segs = [(o + b, o + min(b + TILE_ROWS, M)) for b in range(0, M, TILE_ROWS)]
-    ntt = -(-M // TILE_ROWS)
-    segs += [(o + j * M // ntt, o + (j + 1) * M // ntt) for j in range(ntt)]
+    for rows in (TILE_ROWS, PAIR_TILE_ROWS):
+        ntt = -(-M // rows)
+        segs += [(o + j * M // ntt, o + (j + 1) * M // ntt) for j in range(ntt)]
     return segs
+
+
+def tile_count(M):
+    """Number of tile row ranges of an expert with M rows (see _segments)."""
+    return 2 * -(-M // TILE_ROWS) + -(-M // PAIR_TILE_ROWS)
 
 
 def probe_tokens(ref_idx, E, k, cheap=None):

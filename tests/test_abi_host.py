@@ -134,3 +134,14 @@ def test_decode_rows_setting(L):
     L.moe_set_decode_rows(77)
     assert L.moe_get_decode_rows() == 77
     L.moe_set_decode_rows(-1)
+
+
+def test_pair_gemm_setting(L):
+    assert L.moe_get_pair_gemm() == -1          # the library default
+    for m in (0, 1, 2, 3):
+        L.moe_set_pair_gemm(m)
+        assert L.moe_get_pair_gemm() == m
+    L.moe_set_pair_gemm(7)
+    assert L.moe_get_pair_gemm() == 3           # two bits only
+    L.moe_set_pair_gemm(-5)
+    assert L.moe_get_pair_gemm() == -1

@@ -144,7 +144,8 @@ def test_forward_fp8_full_size_every_tile(moe, T, fmt):
     first and last token of the other popular experts, using only tokens
     whose eight experts are all among the 16 most popular (more if some tile
     has no such token), so that few experts are dequantised on the host."""
-    from full_size_sampling import check_accumulator, fp8_expert_fn, oracle_on_tokens, probe_tokens
+    from full_size_sampling import (check_accumulator, fp8_expert_fn, oracle_on_tokens,
+                                    probe_tokens, tile_count)
     shape = shape_for("dsv3_fp8", T)
     d = make_inputs(shape, seed=0, device="cuda")
     qgu, sgu = moe.quantize_fp8_blocks(d["w_gate_up"], fmt)
@@ -164,9 +165,9 @@ def test_forward_fp8_full_size_every_tile(moe, T, fmt):
         for n_cheap in (16, 24, 32, 48):          # widen until every hot tile is reached
             cheap = set(order[:n_cheap].tolist())
             toks, counts, hot, reached = probe_tokens(ref_idx, shape.E, shape.k, cheap=cheap)
-            if reached == 2 * -(-int(counts[hot]) // 128):
+            if reached == tile_count(int(counts[hot])):
                 break
-        assert hot in cheap and reached == 2 * -(-int(counts[hot]) // 128)
+        assert hot in cheap and reached == tile_count(int(counts[hot]))
     tt = torch.from_numpy(toks).cuda()
     ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
                            fp8_expert_fn(qgu, sgu, qd, sd, fmt))

@@ -92,21 +92,25 @@ def test_dispatch_out_of_range_index_is_reported(moe):
 
 
 # ----------------------------------------------------------------- forward
-# (decode-path row threshold, swap-AB rows-per-expert threshold)
-PATHS = {"rows": (0, 0), "swap": (0, 1 << 20), "decode": (2048, -1)}
+# (decode-path row threshold, swap-AB rows-per-expert threshold, CTA-pair mask)
+PATHS = {"rows": (0, 0, 0), "swap": (0, 1 << 20, 0), "decode": (2048, -1, 0),
+         "pair": (0, -1, 3)}
 
 
 @pytest.fixture
 def path(moe, request):
-    """Force one of the three bf16 paths: grouped GEMMs with token rows as
-    the MMA's M side, grouped GEMMs with weight rows as M (swap-AB), or the
-    decode GEMVs."""
-    dec, swap = PATHS[request.param]
+    """Force one of the bf16 paths: grouped GEMMs with token rows as the
+    MMA's M side, grouped GEMMs with weight rows as M (swap-AB), both grouped
+    GEMMs on CTA pairs (weight rows as M, cta_group::2), or the decode
+    GEMVs."""
+    dec, swap, pair = PATHS[request.param]
     moe.set_decode_rows(dec)
     moe.set_swap_rows(swap)
+    moe.set_pair_gemm(pair)
     yield request.param
     moe.set_decode_rows(-1)
     moe.set_swap_rows(-1)
+    moe.set_pair_gemm(-1)
 
 
 def _forward_case(moe, shape, seed=0, logit_bias=None, device_inputs=None, act="silu"):
@@ -136,7 +140,7 @@ SMALL_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("path", ["rows", "swap", "decode"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap", "pair", "decode"], indirect=True)
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 def test_forward_bf16_parity(moe, shape, path):
     out, ref = _forward_case(moe, shape)
@@ -150,21 +154,51 @@ def test_forward_bf16_down_gemm_phases(moe, phases):
     """The down GEMM's output columns in 2 or 4 slices run one after the
     other (the order used when the fp32 accumulator exceeds L2): every tile
     still runs exactly once."""
+    from full_size_sampling import check_accumulator
+    shape = MoEShape(T=300, H=1024, I=384, E=6, k=3)
     moe.set_down_phases(phases)
     try:
-        out, ref = _forward_case(moe, MoEShape(T=300, H=1024, I=384, E=6, k=3))
+        out, ref = _forward_case(moe, shape)
     finally:
         moe.set_down_phases(-1)
-    assert O.rel_max_err(out, ref) <= BF16_TOL
+    # 307 k outputs: checked on the fp32 accumulator, the bf16 output its
+    # exact RNE image (see tests/full_size_sampling.py)
+    out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
+    check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
 
 
-@pytest.mark.parametrize("path", ["rows", "swap"], indirect=True)
+@pytest.mark.parametrize("mask", [1, 2, 3])
+@pytest.mark.parametrize("group", [0, 1, 2])
+@pytest.mark.parametrize("shape", [
+    MoEShape(T=1200, H=512, I=256, E=2, k=1),     # 600 rows per expert: three 200-token pair tiles
+    MoEShape(T=700, H=256, I=384, E=8, k=3),      # 262 rows per expert on average: ragged pair tiles
+    MoEShape(T=37, H=768, I=128, E=16, k=4),      # 9 rows per expert: 16-column tiles, one half-step
+])
+def test_forward_bf16_pair_gemms(moe, mask, group, shape):
+    """Gate/up (mask 1), down (mask 2) or both on CTA pairs, with the token
+    tiles of an expert in groups of 0 (all), 1 or 2: every tile runs once,
+    both CTAs' halves of the tokens and of the weight rows land in place."""
+    from full_size_sampling import check_accumulator
+    moe.set_decode_rows(0)
+    moe.set_pair_gemm(mask)
+    moe.set_tile_group(group)
+    try:
+        out, ref = _forward_case(moe, shape)
+    finally:
+        moe.set_decode_rows(-1)
+        moe.set_pair_gemm(-1)
+        moe.set_tile_group(-1)
+    out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
+    check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
+
+
+@pytest.mark.parametrize("path", ["rows", "swap", "pair"], indirect=True)
 def test_forward_bf16_parity_qwen_shape_520_tokens(moe, path):
     out, ref = _forward_case(moe, MoEShape(T=520, H=2048, I=1408, E=60, k=4))
     assert O.rel_max_err(out, ref) <= BF16_TOL
 
 
-@pytest.mark.parametrize("path", ["rows", "swap", "decode"], indirect=True)
+@pytest.mark.parametrize("path", ["rows", "swap", "pair", "decode"], indirect=True)
 def test_forward_bf16_one_expert_takes_all(moe, path):
     shape = MoEShape(T=700 if path != "decode" else 90, H=256, I=256, E=8, k=2)
     bias = torch.zeros(8)
@@ -253,12 +287,14 @@ def test_all_paths_agree(moe):
     d = make_inputs(shape, seed=5, device="cuda")
     idx, w = moe.route(d["logits"], shape.k)
     outs = []
-    for dec, swap in PATHS.values():
+    for dec, swap, pair in PATHS.values():
         moe.set_decode_rows(dec)
         moe.set_swap_rows(swap)
+        moe.set_pair_gemm(pair)
         outs.append(moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"]).float())
     moe.set_decode_rows(-1)
     moe.set_swap_rows(-1)
+    moe.set_pair_gemm(-1)
     # every path is within BF16_TOL * rms of the oracle, so two paths agree
     # within twice that (triangle inequality); in practice they differ by a
     # one-ulp bf16 flip at the largest outputs, about 2 % of rms
@@ -313,8 +349,9 @@ def test_forward_bf16_repeatable_and_token_order_equivariant(moe):
     assert (b - ref).abs().max().item() <= 1e-2 * ref.pow(2).mean().sqrt().item()
 
 
-@pytest.mark.parametrize("name,T", [("qwen", 4096), ("dsv3", 8192)])
-def test_forward_bf16_full_size_every_tile(moe, name, T):
+@pytest.mark.parametrize("name,T,pair", [("qwen", 4096, -1), ("dsv3", 8192, -1),
+                                         ("qwen", 4096, 3), ("dsv3", 8192, 3)])
+def test_forward_bf16_full_size_every_tile(moe, name, T, pair):
     """Full workload size on the GPU, through the default path choice; the
     oracle recomputes the tokens at the edges of every grouped-GEMM tile of
     the busiest expert (63 tiles of 128 rows for the skewed DeepSeek-V3
@@ -322,18 +359,21 @@ def test_forward_bf16_full_size_every_tile(moe, name, T):
     fp32 accumulator is checked against it, and the bf16 output against the
     accumulator (bit for bit)."""
     from full_size_sampling import (bf16_expert_fn, check_accumulator, oracle_on_tokens,
-                                    probe_tokens)
+                                    probe_tokens, tile_count)
     shape = shape_for(name, T)
     d = make_inputs(shape, seed=0, device="cuda")
     idx, w = moe.route(d["logits"], shape.k)
-    out = moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"])
-    moe.workspace_status(moe.default_workspace())
+    moe.set_pair_gemm(pair)       # -1: the library's default kernels; 3: both GEMMs on CTA pairs
+    try:
+        out = moe.experts_forward(d["hidden"], idx, w, d["w_gate_up"], d["w_down"])
+        moe.workspace_status(moe.default_workspace())
+    finally:
+        moe.set_pair_gemm(-1)
     ref_idx, ref_w = O.route(d["logits"].cpu().numpy(), shape.k)
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
     np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
     toks, counts, hot, reached = probe_tokens(ref_idx, shape.E, shape.k)
-    n_tiles = 2 * -(-int(counts[hot]) // 128)
-    assert reached == n_tiles
+    assert reached == tile_count(int(counts[hot]))
     tt = torch.from_numpy(toks).cuda()
     ref = oracle_on_tokens(toks, ref_idx, ref_w, d["hidden"][tt].float().cpu().numpy(),
                            bf16_expert_fn(d["w_gate_up"], d["w_down"]))
@@ -387,6 +427,7 @@ def _replay_case(moe, shape, seeds, fp8=None):
 @pytest.mark.parametrize("path,shape", [
     ("rows", MoEShape(T=300, H=256, I=384, E=6, k=3)),
     ("swap", MoEShape(T=300, H=256, I=384, E=6, k=3)),
+    ("pair", MoEShape(T=300, H=256, I=384, E=6, k=3)),
     ("decode", MoEShape(T=4, H=512, I=256, E=16, k=4)),      # the two fused decode kernels
     ("decode", MoEShape(T=40, H=512, I=256, E=16, k=4)),     # dispatch, two GEMVs, combine
 ], indirect=["path"])
