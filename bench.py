@@ -355,6 +355,8 @@ def run_ours(args, rank, world, local_rank):
         moe.set_down_phases(args.down_phases)
     if args.pair_gemm is not None:
         moe.set_pair_gemm(args.pair_gemm)
+    if args.down_l2 is not None:
+        moe.set_down_l2_hints(args.down_l2)
     if args.fp4_gemv_rows is not None:
         moe.set_fp4_gemv_rows(args.fp4_gemv_rows)
     if args.decode_kernels is not None:
@@ -644,6 +646,7 @@ def run_ours(args, rank, world, local_rank):
                    "decode_kernels": 1 if moe.get_decode_single() else 2,
                    "down_phases": moe.get_down_phases(),
                    "pair_gemm": moe.get_pair_gemm(),
+                   "down_l2_hints": moe.get_down_l2_hints(),
                    "activation": args.activation,
                    "scaled_kernels": ("block-scaled tensor-core MMA (kind::mxf8f6f4, UE8M0)"
                                       if mx_path else
@@ -703,6 +706,9 @@ def main():
     ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],
                     help="small bf16 decode batches as one cooperative kernel or two kernels "
                          "(library default)")
+    ap.add_argument("--down-l2", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="down GEMM L2 policies: bit 0 accumulator evict_last, bit 1 weights "
+                         "evict_first (library default)")
     ap.add_argument("--pair-gemm", type=int, default=None, choices=[0, 1, 2, 3],
                     help="bf16 grouped GEMMs on CTA pairs: bit 0 gate/up, bit 1 down "
                          "(library default)")

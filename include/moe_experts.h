@@ -288,6 +288,17 @@ void moe_set_pair_gemm(int mask);
 int moe_get_pair_gemm(void);
 
 /*
+ * moe_set_down_l2_hints - L2 policies of the down GEMMs (bf16 swap-AB and
+ * block-scaled): bit 0 = the fp32 accumulator's reductions evict_last (its
+ * lines kept in preference to streaming data), bit 1 = the W_down tile
+ * loads evict_first.  0: no policy; bits < 0 restore the default, 1 (the
+ * accumulator evict_last, measured 1-3 % faster; bit 1 measured no faster).
+ * Process-wide; moe_get_down_l2_hints returns the bits in use.
+ */
+void moe_set_down_l2_hints(int bits);
+int moe_get_down_l2_hints(void);
+
+/*
  * moe_set_tile_group - tile order of the token-row gate/up GEMMs (bf16 and
  * block-scaled).  Inside an expert the 128-row m-tiles run in groups of m_tiles: every n-tile of one
  * group (m fastest), then the next group, so that an expert with many rows

@@ -22,7 +22,7 @@ __all__ = [
     "get_decode_rows", "set_swap_rows", "get_swap_rows", "profile_begin", "profile_end", "profile_read",
     "selftest_wait_timeout", "launch_count", "accumulator", "set_block_scaled_mma",
     "get_block_scaled_mma", "set_fp4_gemv_rows", "get_fp4_gemv_rows", "set_decode_single",
-    "get_decode_single", "set_tile_group", "get_tile_group", "set_pair_gemm", "get_pair_gemm", "set_down_phases",
+    "get_decode_single", "set_tile_group", "get_tile_group", "set_pair_gemm", "get_pair_gemm", "set_down_l2_hints", "get_down_l2_hints", "set_down_phases",
     "get_down_phases",
     "Workspace", "STATUS", "STAGES", "W_BF16", "W_FP8_E4M3", "W_FP4_E2M1", "SCALE_NONE", "SCALE_F32",
     "SCALE_UE8M0", "ACTIVATIONS",
@@ -71,6 +71,8 @@ _SIGS = {
     "moe_workspace_accumulator_offset": ([_I, _I, _I, _I, _I, _I], _SZ),
     "moe_set_block_scaled_mma": ([_I], None),
     "moe_get_block_scaled_mma": ([], _I),
+    "moe_set_down_l2_hints": ([_I], None),
+    "moe_get_down_l2_hints": ([], _I),
     "moe_set_pair_gemm": ([_I], None),
     "moe_get_pair_gemm": ([], _I),
     "moe_set_down_phases": ([_I], None),
@@ -333,6 +335,16 @@ def set_block_scaled_mma(on: bool):
 
 def get_block_scaled_mma() -> bool:
     return bool(lib().moe_get_block_scaled_mma())
+
+
+def set_down_l2_hints(bits: int):
+    """L2 policies of the down GEMMs: bit 0 accumulator evict_last, bit 1
+    W_down loads evict_first (< 0: the default, 1)."""
+    lib().moe_set_down_l2_hints(int(bits))
+
+
+def get_down_l2_hints() -> int:
+    return int(lib().moe_get_down_l2_hints())
 
 
 def set_pair_gemm(mask: int):

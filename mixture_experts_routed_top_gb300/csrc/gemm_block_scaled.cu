@@ -94,6 +94,7 @@ struct MxDev {
   const float* topk_w;
   int act;
   int group;                // m-tiles per tile group (0: all of the expert's)
+  int l2_hints;             // down: bit 0 accumulator evict_last, bit 1 weights evict_first
   int phases;               // n-tile slices run one after the other (>= 1)
 };
 
@@ -304,7 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(&tm_a, fb, a_dst, ld.kb * BK, ld.arow);
         if (EPI == EPI_SWIGLU_Q)  // 128 gate rows, then their up rows: one 3-D box
           tma_load_3d(&tm_b, fb, b_dst, ld.kb * BK, ld.n * 128, 2 * ld.e);
-        else                      // 256 rows of W_down[e]: one box
+        else if (p.l2_hints & 2)  // 256 rows of W_down[e]: one box
+          tma_load_2d_hint(&tm_b, fb, b_dst, ld.kb * BK, ld.brow0, l2_policy_evict_first());
+        else
           tma_load_2d(&tm_b, fb, b_dst, ld.kb * BK, ld.brow0);
       }
       // this stage's scale factors (loaded kSfAhead iterations ago) into
@@ -477,11 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tok = f / p.k;
           const float wgt = __ldg(p.topk_w + f);
           float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + 128 * half;
+          if (p.l2_hints & 1) {
+            const uint64_t pol = l2_policy_evict_last();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            red_add_v4(orow + 4 * j, wgt * __uint_as_float(v[4 * j]),
-                       wgt * __uint_as_float(v[4 * j + 1]), wgt * __uint_as_float(v[4 * j + 2]),
-                       wgt * __uint_as_float(v[4 * j + 3]));
+            for (int j = 0; j < 32; ++j)
+              red_add_v4_hint(orow + 4 * j, wgt * __uint_as_float(v[4 * j]),
+                              wgt * __uint_as_float(v[4 * j + 1]),
+                              wgt * __uint_as_float(v[4 * j + 2]),
+                              wgt * __uint_as_float(v[4 * j + 3]), pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              red_add_v4(orow + 4 * j, wgt * __uint_as_float(v[4 * j]),
+                         wgt * __uint_as_float(v[4 * j + 1]), wgt * __uint_as_float(v[4 * j + 2]),
+                         wgt * __uint_as_float(v[4 * j + 3]));
+          }
         }
       }
     }
@@ -596,6 +609,7 @@ cudaError_t launch_mx_impl(const GroupedGemmMxArgs& a, cudaStream_t s) {
   p.act = a.act;
   p.group = a.tile_group;
   p.phases = a.phases > 0 ? a.phases : 1;
+  p.l2_hints = a.l2_hints;
   launch_pdl(kern, a.num_sms, kThreads, LM::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

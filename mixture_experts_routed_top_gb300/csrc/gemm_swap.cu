@@ -67,6 +67,7 @@ struct GemmDev {
   const float* topk_w;
   int act;               // moe_activation of the gate/up epilogue
   int phases;            // feature-block slices run one after the other (>= 1)
+  int l2_hints;          // down: bit 0 accumulator evict_last, bit 1 weights evict_first
 };
 
 struct Tile {
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t ph = 0, issued = 0, last_par = 0;
       bool ok = true;
+      const uint64_t pol_first = l2_policy_evict_first();
       // gate/up: feature fb*128 in the [2E, I, H] view of the weights (one
       // 3-D box: 128 gate rows, then their up rows); down: the first of the
       // tile's 128*NA rows of W_down[e] (one box of 128*NA rows)
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
           if (EPI == EPI_SWIGLU) tma_load_3d(&tm_w, fb, a_dst, kb * BK, wrow, 2 * t.e);
+          else if (p.l2_hints & 2) tma_load_2d_hint(&tm_w, fb, a_dst, kb * BK, wrow, pol_first);
           else tma_load_2d(&tm_w, fb, a_dst, kb * BK, wrow);
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(&tm_x, fb, b_dst + b * B_BOX, kb * BK, t.t0 + 64 * b);
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int f = q * 32 + lane;       // feature row within the 128-row box
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint64_t pol_last = l2_policy_evict_last();
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const Tile t = decode_tile(tile, NFT, E, s_off, s_pref, p.phases);
@@ -308,8 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float w = __shfl_sync(0xffffffffu, w_l, i);
             if (i < cnt) {
               float* orow = p.out32 + static_cast<long>(tok) * p.H + col;
-              red_add_f32(orow, w * __uint_as_float(d0[i]));
-              if (NA == 2) red_add_f32(orow + 128, w * __uint_as_float(d1[i]));
+              if (p.l2_hints & 1) {
+                red_add_f32_hint(orow, w * __uint_as_float(d0[i]), pol_last);
+                if (NA == 2) red_add_f32_hint(orow + 128, w * __uint_as_float(d1[i]), pol_last);
+              } else {
+                red_add_f32(orow, w * __uint_as_float(d0[i]));
+                if (NA == 2) red_add_f32(orow + 128, w * __uint_as_float(d1[i]));
+              }
             }
           }
         }
@@ -352,6 +361,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, cudaStream_t s) {
   p.topk_w = a.topk_w;
   p.act = a.act;
   p.phases = a.phases > 0 ? a.phases : 1;
+  p.l2_hints = a.l2_hints;
   launch_pdl(kern, a.num_sms, kThreads, SMEM_BYTES, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

@@ -68,6 +68,7 @@ std::atomic<int> g_fp4_gemv_rows{-1};     // FP4: CUDA-core GEMVs up to this man
 std::atomic<int> g_decode_single{0};      // small decode batches as one cooperative launch
 std::atomic<int> g_tile_group{-1};        // token-row gate/up GEMM: m-tiles per tile group
 std::atomic<int> g_down_phases{-1};       // down GEMMs: accumulator slices (< 0: automatic)
+std::atomic<int> g_down_l2{kDownL2Default};  // down GEMMs: L2 policy bits (accumulator, weights)
 std::atomic<int> g_pair_gemm{-1};         // bf16 grouped GEMMs on CTA pairs (bit mask, < 0: default)
 
 // ----------------------------------------------------------- workspace map
@@ -276,6 +277,9 @@ int moe_get_swap_rows(void) {
   const int r = g_swap_rows.load(std::memory_order_relaxed);
   return r < 0 ? kSwapRowsDefault : r;
 }
+
+void moe_set_down_l2_hints(int bits) { g_down_l2 = bits < 0 ? kDownL2Default : (bits & 3); }
+int moe_get_down_l2_hints(void) { return g_down_l2.load(std::memory_order_relaxed); }
 
 void moe_set_pair_gemm(int mask) { g_pair_gemm = mask < 0 ? -1 : (mask & 3); }
 int moe_get_pair_gemm(void) { return g_pair_gemm.load(std::memory_order_relaxed); }
@@ -539,6 +543,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / 256)));
       g.tile_group = 0;
       g.phases = down_phases(T, H, H / 256, g_down_phases.load(std::memory_order_relaxed));
+      g.l2_hints = moe_get_down_l2_hints();
       if ((e = launch_gemm2_mx(g, fp4, s)) != cudaSuccess) return cuda_fail(e, "gemm2_mx");
     }
     {
@@ -803,6 +808,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     const int nf = (H % 256 == 0) ? 256 : 128;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / nf)));
     g.phases = down_phases(T, H, H / nf, g_down_phases.load(std::memory_order_relaxed));
+    g.l2_hints = moe_get_down_l2_hints();
     e = pair2 ? launch_gemm2_bf16_pair(g, n, s)
               : swap2 ? launch_gemm2_bf16_swap(g, s) : launch_gemm2_bf16_rows(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm2");

@@ -139,6 +139,16 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// The same with an L2 policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap* map, uint32_t bar,
+                                                 uint32_t dst, int x, int y, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor load (coordinates x innermost, then y, z).  Used
 // for the gate/up weights viewed as [2E, I, K]: one box of {x, rows, 2}
 // brings the gate rows and then the matching up rows of one expert.
@@ -149,14 +159,6 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint32_t bar
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) from global memory into L2 (p and bytes
-// multiples of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
-               "r"(bytes)
-               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -482,6 +484,29 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 }
 __device__ __forceinline__ void red_add_f32(float* p, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
+// L2 policies: lines kept in preference to others (evict_last), or the
+// first to go (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// The reductions above with an L2 policy for the accumulator lines.
+__device__ __forceinline__ void red_add_v4_hint(float* p, float a, float b, float c, float d,
+                                                uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+               "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void red_add_f32_hint(float* p, float a, uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(a), "l"(pol)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -130,6 +130,7 @@ struct GroupedGemmArgs {
   int act;                   // moe_activation of the gate/up epilogue
   int tile_group = 0;        // token-row kernel: m-tiles per tile group (0: all)
   int phases = 1;            // swap-AB kernel: feature-block slices run in turn
+  int l2_hints = 0;          // down GEMM: bit 0 accumulator evict_last, bit 1 weights evict_first
 };
 cudaError_t launch_gemm1_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
@@ -147,6 +148,10 @@ cudaError_t launch_gemm2_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaSt
 // slower at H = 2048 (Qwen width, whose ~140-token tiles leave the pair
 // bound by L2 reads); the down GEMM measured slower on pairs everywhere.
 constexpr int kPairGateUpMinH = 4096;
+// Down GEMMs' L2 policies by default: the accumulator's reductions
+// evict_last (measured 1-3 % faster at every prefill size; evict_first on
+// the weight loads measured no faster and is off).
+constexpr int kDownL2Default = 1;
 inline int pair_gemm_default(int H) { return H >= kPairGateUpMinH ? 1 : 0; }
 constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
@@ -184,6 +189,7 @@ struct GroupedGemmFp8Args {
   const float* topk_w;
   int num_sms;
   int act;                   // moe_activation of the gate/up epilogue
+  int l2_hints = 0;          // as GroupedGemmArgs::l2_hints
 };
 cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
 cudaError_t launch_gemm2_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);
@@ -212,6 +218,7 @@ struct GroupedGemmMxArgs {
   int act;
   int tile_group = 0;        // m-tiles per tile group (0: all)
   int phases = 1;            // n-tile slices run in turn
+  int l2_hints = 0;          // as GroupedGemmArgs::l2_hints
 };
 cudaError_t launch_gemm1_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
 cudaError_t launch_gemm2_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);

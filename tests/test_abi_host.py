@@ -145,3 +145,13 @@ def test_pair_gemm_setting(L):
     assert L.moe_get_pair_gemm() == 3           # two bits only
     L.moe_set_pair_gemm(-5)
     assert L.moe_get_pair_gemm() == -1
+
+
+def test_down_l2_hints_setting(L):
+    assert L.moe_get_down_l2_hints() == 1       # accumulator evict_last by default
+    L.moe_set_down_l2_hints(2)
+    assert L.moe_get_down_l2_hints() == 2
+    L.moe_set_down_l2_hints(0)
+    assert L.moe_get_down_l2_hints() == 0
+    L.moe_set_down_l2_hints(-1)
+    assert L.moe_get_down_l2_hints() == 1

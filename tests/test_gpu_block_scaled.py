@@ -168,11 +168,13 @@ def test_fp4_gemv_and_gemm_paths_agree(moe):
 
 @pytest.mark.parametrize("fmt", ["fp4", "fp8"])
 def test_block_scaled_down_gemm_phases_and_groups(moe, fmt):
-    """Down GEMM output columns in four slices and gate/up m-tiles in groups
-    of two (an expert with 5 m-tiles): every tile still runs exactly once."""
+    """Down GEMM output columns in four slices (with L2 policies on its
+    accumulator reductions and weight loads) and gate/up m-tiles in groups of
+    two (an expert with 5 m-tiles): every tile still runs exactly once."""
     shape = MoEShape(T=700, H=1024, I=256, E=2, k=2)
     moe.set_down_phases(4)
     moe.set_tile_group(2)
+    moe.set_down_l2_hints(3)
     try:
         if fmt == "fp4":
             out, ref, _ = _run_fp4(moe, shape)
@@ -181,6 +183,7 @@ def test_block_scaled_down_gemm_phases_and_groups(moe, fmt):
     finally:
         moe.set_down_phases(-1)
         moe.set_tile_group(-1)
+        moe.set_down_l2_hints(-1)
     assert O.rel_max_err(out, ref) <= TOL
 
 

@@ -167,6 +167,21 @@ def test_forward_bf16_down_gemm_phases(moe, phases):
     check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
 
 
+@pytest.mark.parametrize("bits", [1, 2, 3])
+def test_forward_bf16_down_l2_hints(moe, bits):
+    """Down GEMM with L2 policies on the accumulator reductions and/or the
+    weight loads: the same result, checked like any forward."""
+    from full_size_sampling import check_accumulator
+    shape = MoEShape(T=300, H=1024, I=384, E=6, k=3)
+    moe.set_down_l2_hints(bits)
+    try:
+        out, ref = _forward_case(moe, shape)
+    finally:
+        moe.set_down_l2_hints(-1)
+    out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
+    check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
+
+
 @pytest.mark.parametrize("mask", [1, 2, 3])
 @pytest.mark.parametrize("group", [0, 1, 2])
 @pytest.mark.parametrize("shape", [
