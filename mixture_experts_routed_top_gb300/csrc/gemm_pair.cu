@@ -76,6 +76,7 @@ struct PairDev {
   const float* topk_w;
   int act;
   int group;             // token tiles per tile group (0: all of the expert's)
+  int l2_hints;          // down: bit 0 accumulator evict_last
 };
 
 struct Tile {
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const uint64_t pol_last = l2_policy_evict_last();
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int wp = q & 1;              // warp pair (gate/up): quarters wp and wp+2
     const bool upw = q >= 2;
@@ -377,7 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const int tok = __shfl_sync(0xffffffffu, tok_l, i);
             const float w = __shfl_sync(0xffffffffu, w_l, i);
-            if (i < cnt) red_add_f32(p.out32 + static_cast<long>(tok) * p.H + col, w * __uint_as_float(v[i]));
+            if (i < cnt) {
+              float* o = p.out32 + static_cast<long>(tok) * p.H + col;
+              if (p.l2_hints & 1) red_add_f32_hint(o, w * __uint_as_float(v[i]), pol_last);
+              else red_add_f32(o, w * __uint_as_float(v[i]));
+            }
           }
         }
       }
@@ -437,6 +443,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, long tiles_max, cudaStream_t s
   p.topk_w = a.topk_w;
   p.act = a.act;
   p.group = a.tile_group;
+  p.l2_hints = a.l2_hints;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

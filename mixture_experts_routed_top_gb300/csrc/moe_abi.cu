@@ -805,7 +805,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     g.tm_a = (swap2 || pair2) ? &tm_wd : &tm_h;
     g.tm_b = (swap2 || pair2) ? &tm_h : &tm_wd;
     g.K = I;
-    const int nf = (H % 256 == 0) ? 256 : 128;
+    const int nf = (pair2 || H % 256 == 0) ? 256 : 128;
     g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / nf)));
     g.phases = down_phases(T, H, H / nf, g_down_phases.load(std::memory_order_relaxed));
     g.l2_hints = moe_get_down_l2_hints();
