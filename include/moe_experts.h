@@ -259,8 +259,8 @@ void moe_set_swap_rows(int rows_per_expert);
 int moe_get_swap_rows(void);
 
 /*
- * moe_set_down_phases - tile order of the down GEMMs (bf16 swap-AB and
- * block-scaled).  Their combine adds every routed row into the fp32
+ * moe_set_down_phases - tile order of the down GEMMs (bf16 swap-AB,
+ * block-scaled and float32-scale FP8).  Their combine adds every routed row into the fp32
  * accumulator [T, H] of its token; when that accumulator is larger than L2,
  * a token's k contributions, made by different experts at different times,
  * find its lines evicted.  With P phases the output columns are cut into P
@@ -288,8 +288,8 @@ void moe_set_pair_gemm(int mask);
 int moe_get_pair_gemm(void);
 
 /*
- * moe_set_down_l2_hints - L2 policies of the down GEMMs (bf16 swap-AB and
- * block-scaled): bit 0 = the fp32 accumulator's reductions evict_last (its
+ * moe_set_down_l2_hints - L2 policies of the down GEMMs (bf16 swap-AB,
+ * block-scaled and float32-scale FP8; bit 1 only the first two): bit 0 = the fp32 accumulator's reductions evict_last (its
  * lines kept in preference to streaming data), bit 1 = the W_down tile
  * loads evict_first.  0: no policy; bits < 0 restore the default, 1 (the
  * accumulator evict_last, measured 1-3 % faster; bit 1 measured no faster).
@@ -299,9 +299,10 @@ void moe_set_down_l2_hints(int bits);
 int moe_get_down_l2_hints(void);
 
 /*
- * moe_set_tile_group - tile order of the token-row gate/up GEMMs (bf16 and
- * block-scaled).  Inside an expert the 128-row m-tiles run in groups of m_tiles: every n-tile of one
- * group (m fastest), then the next group, so that an expert with many rows
+ * moe_set_tile_group - tile order of the token-row gate/up GEMMs (bf16,
+ * block-scaled and float32-scale FP8; for the CTA-pair kernel, its 256-token
+ * tiles).  Inside an expert the 128-row m-tiles run in groups of m_tiles:
+ * every n-tile of one group (m fastest), then the next group, so that an expert with many rows
  * re-reads one group's activation tiles per n-tile instead of all of them.
  * 0 puts all of an expert's m-tiles in one group; m_tiles < 0 restores the
  * default (4, measured 2 % faster than one group on the skewed

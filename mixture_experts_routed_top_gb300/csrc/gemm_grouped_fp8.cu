@@ -78,11 +78,23 @@ struct Fp8Dev {
   const int* sorted_f;
   const float* topk_w;
   int act;              // moe_activation of the gate/up epilogue
+  int group;            // m-tiles per tile group (0: all of the expert's)
+  int phases;           // n-tile slices run one after the other (>= 1)
+  int l2_hints;         // down: bit 0 accumulator evict_last
 };
 
-__device__ __forceinline__ void decode_tile8(int tile, int NT, int E, const int* s_pref, int& e,
-                                             int& m, int& n) {
-  const int v = tile / NT;
+// Tile -> (expert e, m-tile m, n-tile n).  The n-tiles are cut into
+// `phases` equal slices run one after the other (the down GEMM's combine
+// then touches a [T, H / phases] slice of the fp32 accumulator at a time);
+// inside a slice and an expert the m-tiles run in groups of `group` (0:
+// all), a group's tiles for every n-tile of the slice, m fastest.
+__device__ __forceinline__ void decode_tile8(int tile, int NT, int E, const int* s_pref,
+                                             int group, int phases, int& e, int& m, int& n) {
+  const int ntp = NT / phases;
+  const int per_phase = s_pref[E] * ntp;
+  const int ph = tile / per_phase;
+  tile -= ph * per_phase;
+  const int v = tile / ntp;
   int lo = 0, hi = E;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -91,9 +103,13 @@ __device__ __forceinline__ void decode_tile8(int tile, int NT, int E, const int*
   }
   e = lo;
   const int mt = s_pref[e + 1] - s_pref[e];
-  const int local = tile - s_pref[e] * NT;
-  n = local / mt;
-  m = local - n * mt;
+  const int local = tile - s_pref[e] * ntp;
+  const int G = (group > 0 && group < mt) ? group : mt;
+  const int g = local / (G * ntp);
+  const int gg = min(G, mt - g * G);
+  const int r = local - g * G * ntp;
+  n = ph * ntp + r / gg;
+  m = g * G + (r - (r / gg) * gg);
 }
 
 __device__ __forceinline__ float load_scale(const void* base, long i, int ue8m0) {
@@ -178,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, m, n;
-        decode_tile8(tile, NT, E, s_pref, e, m, n);
+        decode_tile8(tile, NT, E, s_pref, p.group, p.phases, e, m, n);
         const int arow = s_off[e] + m * BM;
         // gate/up: feature n*128 in the [2E, I, H] view; down: the first of
         // the tile's 256 rows of W_down[e]
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, m, n;
-      decode_tile8(tile, NT, E, s_pref, e, m, n);
+      decode_tile8(tile, NT, E, s_pref, p.group, p.phases, e, m, n);
       const int m_e = s_off[e + 1] - s_off[e];
       const bool valid = m * BM + r < m_e;
       const long R = static_cast<long>(s_off[e]) + m * BM + r;
@@ -429,14 +445,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tok = f / p.k;
           const float wgt = __ldg(p.topk_w + f);
           float* orow = p.out32 + static_cast<long>(tok) * p.H + n * BN + col0;
+          if (p.l2_hints & 1) {
+            const uint64_t pol = l2_policy_evict_last();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            red_add_v4(orow + 4 * j, wgt * acc0[4 * j], wgt * acc0[4 * j + 1],
-                       wgt * acc0[4 * j + 2], wgt * acc0[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+              red_add_v4_hint(orow + 4 * j, wgt * acc0[4 * j], wgt * acc0[4 * j + 1],
+                              wgt * acc0[4 * j + 2], wgt * acc0[4 * j + 3], pol);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            red_add_v4(orow + 32 + 4 * j, wgt * acc1[4 * j], wgt * acc1[4 * j + 1],
-                       wgt * acc1[4 * j + 2], wgt * acc1[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+              red_add_v4_hint(orow + 32 + 4 * j, wgt * acc1[4 * j], wgt * acc1[4 * j + 1],
+                              wgt * acc1[4 * j + 2], wgt * acc1[4 * j + 3], pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              red_add_v4(orow + 4 * j, wgt * acc0[4 * j], wgt * acc0[4 * j + 1],
+                         wgt * acc0[4 * j + 2], wgt * acc0[4 * j + 3]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              red_add_v4(orow + 32 + 4 * j, wgt * acc1[4 * j], wgt * acc1[4 * j + 1],
+                         wgt * acc1[4 * j + 2], wgt * acc1[4 * j + 3]);
+          }
         }
       }
     }
@@ -481,6 +509,9 @@ cudaError_t launch_fp8_impl(const GroupedGemmFp8Args& a, cudaStream_t s) {
   p.sorted_f = a.sorted_f;
   p.topk_w = a.topk_w;
   p.act = a.act;
+  p.group = a.tile_group;
+  p.phases = a.phases > 0 ? a.phases : 1;
+  p.l2_hints = a.l2_hints;
   launch_pdl(kern, a.num_sms, kThreads, L8::SMEM, s, *a.tm_a, *a.tm_b, p);
   count_launches(1);
   return cudaGetLastError();

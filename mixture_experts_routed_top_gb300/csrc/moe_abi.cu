@@ -705,6 +705,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       g.a_scale = xs;
       g.w_scale = scale_gate_up;
       g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (I / 128)));
+      g.tile_group = moe_get_tile_group();
       if ((e = launch_gemm1_fp8(g, s)) != cudaSuccess) return cuda_fail(e, "gemm1_fp8");
     }
     {
@@ -715,6 +716,9 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       g.a_scale = hs;
       g.w_scale = scale_down;
       g.num_sms = static_cast<int>(std::min<long>(sms, mtiles_max * (H / 256)));
+      g.tile_group = 0;
+      g.phases = down_phases(T, H, H / 256, g_down_phases.load(std::memory_order_relaxed));
+      g.l2_hints = moe_get_down_l2_hints();
       if ((e = launch_gemm2_fp8(g, s)) != cudaSuccess) return cuda_fail(e, "gemm2_fp8");
     }
     {

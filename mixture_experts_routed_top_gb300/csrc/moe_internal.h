@@ -189,6 +189,8 @@ struct GroupedGemmFp8Args {
   const float* topk_w;
   int num_sms;
   int act;                   // moe_activation of the gate/up epilogue
+  int tile_group = 0;        // m-tiles per tile group (0: all)
+  int phases = 1;            // n-tile slices run in turn
   int l2_hints = 0;          // as GroupedGemmArgs::l2_hints
 };
 cudaError_t launch_gemm1_fp8(const GroupedGemmFp8Args& a, cudaStream_t s);

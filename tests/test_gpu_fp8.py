@@ -108,6 +108,23 @@ def test_forward_fp8_parity(moe, shape, fmt):
     assert O.rel_max_err(out, plain) < 0.5
 
 
+def test_forward_fp8_f32_phases_groups_l2_hints(moe):
+    """Float32-scale kernel with its down GEMM's output columns in four
+    slices (accumulator reductions under the L2 policy) and gate/up m-tiles
+    in groups of two (an expert with 5 m-tiles): every tile runs once."""
+    shape = MoEShape(T=700, H=1024, I=256, E=2, k=2)
+    moe.set_down_phases(4)
+    moe.set_tile_group(2)
+    moe.set_down_l2_hints(1)
+    try:
+        out, ref, _ = _fp8_case(moe, shape, "f32")
+    finally:
+        moe.set_down_phases(-1)
+        moe.set_tile_group(-1)
+        moe.set_down_l2_hints(-1)
+    assert O.rel_max_err(out, ref) <= FP8_TOL
+
+
 @pytest.mark.parametrize("fmt,act", [("f32", "gelu"), ("ue8m0", "relu")])
 @pytest.mark.parametrize("shape", [MoEShape(T=300, H=512, I=384, E=6, k=3),
                                    MoEShape(T=40, H=1024, I=512, E=64, k=6)])
