@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restric
 #pragma unroll
     for (int i = 0; i < kGatherBatch; ++i) {
       const int c = c0 + 32 * i;
-      if (c < H8) dst[c] = v[i];
+      if (c < H8) __stcs(dst + c, v[i]);   // streaming: the rows are read back once
     }
   }
 }
