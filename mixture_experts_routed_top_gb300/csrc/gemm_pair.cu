@@ -16,9 +16,9 @@
 // Inside an expert the token tiles run in groups of `group`: every feature
 // block of one group (token tile fastest), then the next group.
 //
-// Gate/up GEMM: fb covers 128 features of I; CTA r loads, as one 3-D box
-//   of the weights viewed as [2E, I, H], the gate rows of features
-//   f0..f0+63 and their up rows (f0 = 128 fb + 64 r).  So TMEM lane quarter p (p = 0, 1) holds gate and
+// Gate/up GEMM: fb covers 128 features of I; CTA r loads, as one box of
+//   the weights viewed as [2E, I, H], the gate rows of features f0..f0+63
+//   and their up rows (f0 = 128 fb + 64 r).  So TMEM lane quarter p (p = 0, 1) holds gate and
 //   quarter p+2 up of the same 32 features; the two epilogue warps of such a
 //   pair swap half of their columns through shared memory (the gate warp
 //   computes h for the first 16 tokens of each 32-column step, the up warp
@@ -27,8 +27,13 @@
 //   thread = output feature, the routing-weighted outputs are added into
 //   the fp32 accumulator row of each token (coalesced fp32 reductions).
 //
-// Roles in each CTA (192 threads): warp 0 TMA producer (6-stage ring of
-// 16 KB weights + 16 KB tokens, one 128-row token box per stage), warp 1 TMEM (512 columns, allocated
+// Stages cover 128 of K as two 64-wide swizzled slices: one TMA box per
+// operand and stage (the weights' [2E, I, K] view and the tokens' [n, K]
+// view with the K slice as the outermost coordinate), which halves the TMA
+// operations and barrier hand-offs per byte against 64-wide stages.
+//
+// Roles in each CTA (192 threads): warp 0 TMA producer (3-stage ring of
+// 32 KB weights + 32 KB tokens), warp 1 TMEM (512 columns, allocated
 // by the pair together) and, on rank 0, the MMA issuer (two 256-column
 // accumulator buffers), warps 2-5 epilogue.  Both CTAs' loads complete on
 // rank 0's stage barrier; rank 0's commits arrive on the stage-free and
@@ -43,12 +48,14 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;                   // bf16 elements per 128-byte swizzled row
-constexpr int kStages = 6;
+constexpr int KA = 2;                    // swizzle atoms (64-wide K slices) per stage
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kBufCols = 256;            // one accumulator buffer: N <= 256 columns
-constexpr int A_BYTES = 128 * BK * 2;    // this CTA's 128 weight rows
-constexpr int B_BYTES = 128 * BK * 2;    // one box of 128 token rows
+constexpr int ATOM = 128 * BK * 2;       // 128 rows x one 64-wide K slice: 16 KB
+constexpr int A_BYTES = KA * ATOM;       // this CTA's 128 weight rows, 128 of K
+constexpr int B_BYTES = KA * ATOM;       // 128 token rows, 128 of K
 constexpr int kXStride = 17;             // floats per exchange row: 16 values + 1 (no bank conflicts)
 constexpr int kXBuf = 32 * kXStride;     // floats: one direction, one warp pair, one parity
 constexpr int kTempty = 8;               // epilogue warps of both CTAs
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int NFB = (EPI == EPI_SWIGLU) ? p.I / 128 : p.H / 256;
   const int total = s_pref[E] * NFB;
-  const int KB = p.K / BK;
+  const int KB = p.K / (KA * BK);          // stages per tile (128 of K each)
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -217,11 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb_lead = mapa_shared(fb_local, 0);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          if (EPI == EPI_SWIGLU)  // gate rows f0..f0+63, then their up rows: one 3-D box
-            tma_load_3d_pair(&tm_w, fb_lead, a_dst, kb * BK, arow[0], 2 * t.e);
+          // one box per operand covers both 64-wide K slices of the stage
+          // (the last coordinate counts 64-wide slices along K)
+          if (EPI == EPI_SWIGLU)  // gate rows f0..f0+63, then their up rows, per K slice
+            tma_load_4d_pair(&tm_w, fb_lead, a_dst, 0, arow[0], 2 * t.e, KA * kb);
           else
-            tma_load_2d_pair(&tm_w, fb_lead, a_dst, kb * BK, arow[0]);
-          tma_load_2d_pair(&tm_x, fb_lead, b_dst, kb * BK, brow);
+            tma_load_3d_pair(&tm_w, fb_lead, a_dst, 0, arow[0], KA * kb);
+          tma_load_3d_pair(&tm_x, fb_lead, b_dst, 0, brow, KA * kb);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (ph << stage);
           if (++stage == kStages) {
@@ -271,9 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
           const uint64_t bd = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16_pair(tmem + acc * kBufCols, ad + 2 * kk, bd + 2 * kk, idesc,
+          for (int kk = 0; kk < KA * BK / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * ATOM >> 4) + 2 * (kk & 3);  // K slice, then 16 of K
+            umma_f16_pair(tmem + acc * kBufCols, ad + off, bd + off, idesc,
                           (kb | kk) != 0 ? 1u : 0u);
+          }
           umma_commit_pair_both(smem_u32(&empty[stage]));
           if (++stage == kStages) {
             stage = 0;
@@ -466,8 +477,9 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, long tiles_max, cudaStream_t s
 
 }  // namespace
 
-// tm_a: weights (gate/up: the [2E, I, H] view with boxes {64, 64, 2};
-// down: 128-row boxes), tm_b: activations (128-row boxes), rows of 64 bf16.
+// tm_a: weights (gate/up: the [2E, I, H] view, boxes of 64 gate + 64 up
+// rows; down: 128-row boxes), tm_b: activations (128-row boxes), each box
+// two 64-wide K slices (maps made by the library's 128-wide-K map builder).
 cudaError_t launch_gemm1_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaStream_t s) {
   return launch_impl<EPI_SWIGLU>(a, (n_rows / 256 + a.E) * (a.I / 128), s);
 }

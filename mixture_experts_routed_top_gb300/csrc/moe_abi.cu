@@ -179,6 +179,30 @@ moe_status make_map_gate_up(CUtensorMap* m, const void* base, CUtensorMapDataTyp
   return MOE_OK;
 }
 
+// bf16 operand of the CTA-pair kernel, whose stages cover 128 of K as two
+// 64-wide slices: the matrix [.., K] viewed with the 64-wide K slice index as
+// the outermost coordinate (stride 128 bytes), so one box of
+// {64, rows, (2 planes,) 2 slices} lands as the two swizzled slices one after
+// the other.  rows_dim = the row count, planes = 0 for a plain [rows, K]
+// matrix or 2E for the gate/up weights' [2E, I, K] view (rows_dim = I).
+moe_status make_map_k2(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows_dim,
+                       uint64_t planes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t row_bytes = K * 2;
+  cuuint64_t dims[4] = {64, rows_dim, planes ? planes : K / 64, K / 64};
+  cuuint64_t strides[3] = {row_bytes, planes ? row_bytes * rows_dim : 128, 128};
+  cuuint32_t box[4] = {64, box_rows, 2, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const cuuint32_t rank = planes ? 4 : 3;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (128-wide K stages) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 // 2-D packed e2m1 matrix [rows, k_elems] (two codes per byte, row stride
 // k_elems/2 bytes), box 128 elements x box_rows rows, expanded by TMA into the
 // one-byte-per-element-slot shared-memory form (16 codes in 8 bytes, 8 bytes
@@ -756,16 +780,28 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   const uint32_t xb2 = (pair2 || swap2) ? 128 : rb;
   CUtensorMap tm_x, tm_wgu, tm_h, tm_wd;
   moe_status st;
-  if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, xr1, xb1)) != MOE_OK)
-    return st;
-  if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, I, E, wr1,
-                             xb1 / 2, static_cast<uint64_t>(H) * 2)) != MOE_OK)
-    return st;
-  if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, xr2, xb2)) != MOE_OK)
-    return st;
-  if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
-                     static_cast<uint64_t>(E) * H, wr2, xb2)) != MOE_OK)
-    return st;
+  if (pair1) {  // 128-wide K stages
+    if ((st = make_map_k2(&tm_x, xa, H, n, 0, 128)) != MOE_OK) return st;
+    if ((st = make_map_k2(&tm_wgu, w_gate_up, H, I, static_cast<uint64_t>(E) * 2, 64)) != MOE_OK)
+      return st;
+  } else {
+    if ((st = make_map(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n, xr1, xb1)) != MOE_OK)
+      return st;
+    if ((st = make_map_gate_up(&tm_wgu, w_gate_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, I, E, wr1,
+                               xb1 / 2, static_cast<uint64_t>(H) * 2)) != MOE_OK)
+      return st;
+  }
+  if (pair2) {  // 128-wide K stages
+    if ((st = make_map_k2(&tm_h, hb, I, n, 0, 128)) != MOE_OK) return st;
+    if ((st = make_map_k2(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, 0, 128)) != MOE_OK)
+      return st;
+  } else {
+    if ((st = make_map(&tm_h, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I, n, xr2, xb2)) != MOE_OK)
+      return st;
+    if ((st = make_map(&tm_wd, w_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, I,
+                       static_cast<uint64_t>(E) * H, wr2, xb2)) != MOE_OK)
+      return st;
+  }
 
   {
     StageScope sc(s, MOE_STAGE_DISPATCH);

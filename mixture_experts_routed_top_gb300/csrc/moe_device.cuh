@@ -355,6 +355,14 @@ __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* map, uint32_
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_pair(const CUtensorMap* map, uint32_t bar,
+                                                 uint32_t dst, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
 // Warp-wide, one warp in each CTA of the pair together: the same `ncols`
 // TMEM columns in both CTAs, address written to each CTA's smem `dst`.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
