@@ -11,6 +11,15 @@
 // accumulators with the block's scale product.  Two 256-column TMEM buffers
 // let the MMA of K-block kb+1 run while K-block kb is being promoted.
 //
+// The promotion is what bounds this kernel: every K-block each epilogue
+// thread reads 64 partial sums in four rounds of two 8-column TMEM loads
+// (64 register accumulators and the 96-register ceiling of 18 warps leave
+// room for no more) and folds them in with one fused multiply-add each.  Per
+// K-block a thread loads its three scales for the next K-block (the row's
+// activation scale, and the two weight-block scales at one address across
+// the warp); one thread waits for the partial buffer and the others block
+// on a named barrier rather than polling it.
+//
 // Roles (persistent, one CTA per SM, 576 threads):
 //   warp 0       TMA producer, 4-stage ring of A 128x128 B + B 256x128 B
 //   warp 1       TMEM allocator + MMA issuer
@@ -25,7 +34,10 @@
 //     down:      warpgroup g owns output columns 64g..64g+63 (inside weight
 //                block row g/2); at tile end y * routing weight is added into
 //                the fp32 accumulator of the token (vector reductions)
-// All waits are bounded as in the bf16 kernel.
+// All mbarrier waits are bounded as in the bf16 kernel.  The epilogue's
+// named barriers (one per K-block, one per gate/up tile for the row maxima)
+// cannot be left waiting: the epilogue warps leave their loops only on the
+// decision one thread publishes for the K-block, which all of them read.
 #include <cuda_fp8.h>
 
 #include <atomic>
@@ -126,7 +138,7 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
-template <int EPI>
+template <int EPI, int UE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_b, const Fp8Dev p) {
@@ -141,9 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pfull = bars + 2 * kStages;
   uint64_t* pempty = pfull + 2;
   uint64_t* fin = pempty + 2;
-  uint64_t* amax_bar = fin + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L8::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L8::OFF_MISC + 4);
+  volatile int* s_pok = reinterpret_cast<volatile int*>(smem + L8::OFF_MISC + 8);  // [2]
   float* s_amax = reinterpret_cast<float*>(smem + L8::OFF_AMAX);
   int* s_off = reinterpret_cast<int*>(smem + L8::OFF_OFF);
   int* s_pref = reinterpret_cast<int*>(smem + L8::OFF_PREF);
@@ -161,7 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&pempty[b]), kEpiWarps);
     }
     mbar_init(smem_u32(fin), 1);
-    mbar_init(smem_u32(amax_bar), kEpiWarps * 32);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -300,82 +311,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc0[32], acc1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc0[i] = acc1[i] = 0.f;
-      // Scales of K-blocks kb0..kb0+3: the row's activation scales with one
-      // vector load, the tile's weight-block scales by lanes 0-7 of the warp
-      // (broadcast by shuffle); loaded one group ahead of their use.
-      const int sstride = scale_stride(KBn);
-      const long arow_base = R * sstride;
-      auto load_group = [&](int kb0, float (&sa4)[4], float& wl) {
-        sa4[0] = sa4[1] = sa4[2] = sa4[3] = 0.f;
-        wl = 0.f;
-        if (kb0 >= KB) return;
-        if (valid) {
-          if (p.ue8m0) {
-            const uint32_t b4 = __ldg(reinterpret_cast<const uint32_t*>(
-                static_cast<const uint8_t*>(p.a_scale) + arow_base + kb0));
+      // Scales of K-block kb + 1 are loaded while K-block kb is promoted:
+      // the row's activation scale and the weight-block scales (one address
+      // across the warp, a broadcast load).
+      const long a_base = R * scale_stride(KBn);
+      const long w0_base = wrow0 * KBn, w1_base = wrow1 * KBn;
+      float sa = valid ? load_scale(p.a_scale, a_base, UE) : 0.f;
+      float sw0 = load_scale(p.w_scale, w0_base, UE);
+      float sw1 = (EPI == EPI_SWIGLU_Q) ? load_scale(p.w_scale, w1_base, UE) : sw0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const float s0 = sa * sw0;
+        const float s1 = (EPI == EPI_SWIGLU_Q) ? sa * sw1 : s0;
+        if (kb + 1 < KB) {
+          sa = valid ? load_scale(p.a_scale, a_base + kb + 1, UE) : 0.f;
+          sw0 = load_scale(p.w_scale, w0_base + kb + 1, UE);
+          if (EPI == EPI_SWIGLU_Q) sw1 = load_scale(p.w_scale, w1_base + kb + 1, UE);
+        }
+        const int b = g & 1;
+        // One thread waits for the partial sums and publishes the outcome in
+        // this K-block's slot; the other epilogue warps block on a named
+        // barrier instead of polling the mbarrier, and all of them take the
+        // same decision (the slot is rewritten only after every warp has
+        // passed the next barrier, so no reader sees a later value).
+        if (warp == 2 && lane == 0)
+          s_pok[b] = mbar_wait_bounded(smem_u32(&pfull[b]), (g >> 1) & 1, s_abort, p.err,
+                                       ERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+        named_bar_sync(1, kEpiWarps * 32);
+        if (!s_pok[b]) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t bb = (b4 >> (8 * u)) & 0xFFu;
-              sa4[u] = bb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(bb << 23);
-            }
-          } else {
-            const float4 f4 = __ldg(reinterpret_cast<const float4*>(
-                static_cast<const float*>(p.a_scale) + arow_base + kb0));
-            sa4[0] = f4.x;
-            sa4[1] = f4.y;
-            sa4[2] = f4.z;
-            sa4[3] = f4.w;
+        for (int h = 0; h < 4; ++h) {
+          uint32_t v0[8], v1[8];
+          tmem_ld_32x32b_x8(tb + col0 + 8 * h, v0);
+          tmem_ld_32x32b_x8(tb + col1 + 8 * h, v1);
+          tmem_ld_wait_x8x2(v0, v1);
+          if (h == 3) {  // buffer fully read: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc0[8 * h + i] = fmaf(__uint_as_float(v0[i]), s0, acc0[8 * h + i]);
+            acc1[8 * h + i] = fmaf(__uint_as_float(v1[i]), s1, acc1[8 * h + i]);
           }
         }
-        const int u = lane & 3;
-        if (lane < 8 && kb0 + u < KB)
-          wl = load_scale(p.w_scale, (lane < 4 ? wrow0 : wrow1) * KBn + kb0 + u, p.ue8m0);
-      };
-      float sa_c[4], sa_n[4], w_c, w_n;
-      load_group(0, sa_c, w_c);
-      for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
-        load_group(kb0 + 4, sa_n, w_n);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float sw0 = __shfl_sync(0xffffffffu, w_c, u);
-          const float sw1 = __shfl_sync(0xffffffffu, w_c, 4 + u);
-          if (kb0 + u >= KB) break;
-          const float s0 = sa_c[u] * sw0;
-          const float s1 = (EPI == EPI_SWIGLU_Q) ? sa_c[u] * sw1 : s0;
-          const int b = g & 1;
-          int w_ok = 1;
-          if (lane == 0)
-            w_ok = mbar_wait_bounded(smem_u32(&pfull[b]), (g >> 1) & 1, s_abort, p.err,
-                                     ERR_TIMEOUT_EPILOGUE);
-          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-          if (!w_ok) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tb = tmem + b * kBufCols + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            uint32_t v0[8], v1[8];
-            tmem_ld_32x32b_x8(tb + col0 + 8 * h, v0);
-            tmem_ld_32x32b_x8(tb + col1 + 8 * h, v1);
-            tmem_ld_wait();
-            if (h == 3) {  // buffer fully read: the MMA may reuse it
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&pempty[b]));
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              acc0[8 * h + i] = fmaf(__uint_as_float(v0[i]), s0, acc0[8 * h + i]);
-              acc1[8 * h + i] = fmaf(__uint_as_float(v1[i]), s1, acc1[8 * h + i]);
-            }
-          }
-          ++g;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sa_c[u] = sa_n[u];
-        w_c = w_n;
+        ++g;
       }
       if (!ok) break;
 
@@ -390,26 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* am = s_amax + (amax_phase ? kEpiGroups * 128 : 0);   // double-buffered by tile
         am[wg * 128 + r] = amax;
-        mbar_arrive(smem_u32(amax_bar));
-        int a_ok = 1;
-        if (lane == 0)
-          a_ok = mbar_wait_bounded(smem_u32(amax_bar), amax_phase, s_abort, p.err,
-                                   ERR_TIMEOUT_EPILOGUE);
-        a_ok = __shfl_sync(0xffffffffu, a_ok, 0);
-        if (!a_ok) {
-          ok = false;
-          break;
-        }
+        // every epilogue warp reaches this barrier: their only exits are the
+        // K-block decisions above, which all of them take together
+        named_bar_sync(1, kEpiWarps * 32);
         amax = am[r];
 #pragma unroll
         for (int j = 1; j < kEpiGroups; ++j) amax = fmaxf(amax, am[j * 128 + r]);
         amax_phase ^= 1u;
         // scale as in the weight quantiser: amax/448 or its power-of-two ceiling
         float sc = 1.0f;
-        uint32_t stored = p.ue8m0 ? 127u : __float_as_uint(1.0f);
+        uint32_t stored = UE ? 127u : __float_as_uint(1.0f);
         if (amax != 0.f) {
           const float qv = amax / 448.0f;
-          if (!p.ue8m0) {
+          if (!UE) {
             sc = qv;
             stored = __float_as_uint(qv);
           } else {
@@ -435,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (wg == 0) {
             const long si = R * scale_stride(p.I / 128) + n;
-            if (p.ue8m0) static_cast<uint8_t*>(p.hs)[si] = static_cast<uint8_t>(stored);
+            if (UE) static_cast<uint8_t*>(p.hs)[si] = static_cast<uint8_t>(stored);
             else static_cast<uint32_t*>(p.hs)[si] = stored;
           }
         }
@@ -478,17 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int EPI>
 cudaError_t launch_fp8_impl(const GroupedGemmFp8Args& a, cudaStream_t s) {
-  auto kern = grouped_gemm_fp8_kernel<EPI>;
+  auto kern = a.ue8m0 ? grouped_gemm_fp8_kernel<EPI, 1> : grouped_gemm_fp8_kernel<EPI, 0>;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   // one flag per device; any host thread may launch, so the flags are atomic
   // (setting the attribute twice is harmless, reading a torn flag is not)
-  static std::atomic<bool> attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
+  static std::atomic<bool> attr_set[2][64] = {};
+  std::atomic<bool>* flag = &attr_set[a.ue8m0 ? 1 : 0][dev < 64 ? dev : 0];
+  if (dev >= 64 || !flag->load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L8::SMEM);
     if (err != cudaSuccess) return err;
-    attr_set[dev].store(true, std::memory_order_release);
+    if (dev < 64) flag->store(true, std::memory_order_release);
   }
   Fp8Dev p;
   p.offsets = a.offsets;

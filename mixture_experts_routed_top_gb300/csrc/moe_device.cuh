@@ -431,6 +431,17 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.wait::ld that also names the two 8-column loads it completes, so no
+// use of their registers can be scheduled above the wait.
+__device__ __forceinline__ void tmem_ld_wait_x8x2(uint32_t (&a)[8], uint32_t (&b)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
+                 "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7])
+               :
+               : "memory");
+}
+
 // ---------------------------------------------------------------- misc
 // silu(g) = g / (1 + e^-g).  The fast division (2 ulp of fp32 for divisors
 // below 2^126) replaces the IEEE one: the result is rounded to bf16 or
