@@ -105,3 +105,33 @@ def test_oracle_sample_runs_on_every_weight_format(wfmt):
     smp = bench.OracleSample(w, 4)
     assert smp.n == 4
     assert smp.run() > 0.0
+
+
+def test_dominant_roof_is_the_one_that_binds():
+    """The roofline time is max(flops / tensor peak, bytes / HBM bandwidth):
+    the Qwen-shaped gate/up GEMM (E=60, every expert touched) moves more
+    bytes than its flops take at the tensor peak, the DeepSeek-V3-shaped one
+    the reverse; decode batches stream weights."""
+    peaks = {"hbm_gbs": 6705.2, "bf16_tflops": 1886.7}
+
+    def roof(sname, T, wfmt, sfmt, dominant, touched):
+        w = _w(sname, T, wfmt, sfmt)
+        s = w["shape"]
+        counts = np.zeros(s.E, np.int64)
+        counts[:touched] = 1
+        flops, wbytes, _, _ = bench.algorithmic(w, counts)
+        return bench.dominant_roof(w, dominant, flops, wbytes, peaks), w["shape"]
+
+    (f, b, wb, pk, hbm), s = roof("qwen", 4096, "bf16", None, "gemm1", 60)
+    assert f == 4.0 * s.H * s.I * s.T * s.k
+    # weights (gate and up rows of 60 experts), X rows in, h rows out
+    assert b == 60 * 2 * s.H * s.I * 2 + s.T * s.k * (s.H + s.I) * 2
+    assert hbm and pk == 1886.7
+    (f, b, wb, pk, hbm), s = roof("dsv3", 8192, "bf16", None, "gemm1", 192)
+    assert not hbm
+    (f, b, wb, pk, hbm), s = roof("dsv3", 8192, "bf16", None, "gemm2", 192)
+    assert b == 192 * s.H * s.I * 2 + s.T * s.k * s.I * 2 + s.T * s.H * 4
+    (f, b, wb, pk, hbm), s = roof("qwen", 32, "bf16", None, "gemm1", 50)
+    assert hbm
+    (f, b, wb, pk, hbm), s = roof("dsv3_fp8", 16384, "fp8", "f32", "gemm1", 214)
+    assert not hbm and pk == 2 * 1886.7
