@@ -387,6 +387,8 @@ def run_ours(args, rank, world, local_rank):
         moe.set_fp4_gemv_rows(args.fp4_gemv_rows)
     if args.decode_kernels is not None:
         moe.set_decode_single(args.decode_kernels == 1)
+    if args.decode_rows is not None:
+        moe.set_decode_rows(args.decode_rows)
     w = build_workload(args.workload, dev)
     w["act"] = args.activation
     s = w["shape"]
@@ -665,6 +667,7 @@ def run_ours(args, rank, world, local_rank):
                    "experts_touched": touched, "max_expert_rows": int(counts.max()),
                    "bf16_gemm": args.bf16_gemm, "tile_group": moe.get_tile_group(),
                    "decode_kernels": 1 if moe.get_decode_single() else 2,
+                   "decode_rows": moe.get_decode_rows(),
                    "down_phases": moe.get_down_phases(),
                    "pair_gemm": moe.get_pair_gemm(),
                    "down_l2_hints": moe.get_down_l2_hints(),
@@ -727,6 +730,9 @@ def main():
     ap.add_argument("--decode-kernels", type=int, default=None, choices=[1, 2],
                     help="small bf16 decode batches as one cooperative kernel or two kernels "
                          "(library default)")
+    ap.add_argument("--decode-rows", type=int, default=None,
+                    help="routed rows at or below which the bf16 decode GEMVs run "
+                         "(library default 16)")
     ap.add_argument("--down-l2", type=int, default=None, choices=[0, 1, 2, 3],
                     help="down GEMM L2 policies: bit 0 accumulator evict_last, bit 1 weights "
                          "evict_first (library default)")
