@@ -337,16 +337,8 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
-// Tiled load into this CTA's shared memory whose completion is counted on
+// Tiled loads into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (`bar`: shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar,
-                                                 uint32_t dst, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* map, uint32_t bar,
                                                  uint32_t dst, int x, int y, int z) {
   asm volatile(
