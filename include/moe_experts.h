@@ -281,7 +281,9 @@ int moe_get_down_phases(void);
  * GEMM, bit 1: the down GEMM (only where H % 256 == 0; else the one-CTA
  * kernel runs); mask < 0 restores the default: gate/up on pairs where
  * H >= 4096 (measured faster at DeepSeek-V3 width, slower at H = 2048), the
- * down GEMM on one-CTA kernels (measured faster at every size).
+ * down GEMM on pairs where T*k >= 8*E, i.e. at least 8 routed rows per
+ * expert on average (measured faster there; the one-CTA swap-AB kernel is
+ * faster for smaller batches).
  * Process-wide; moe_get_pair_gemm returns the mask set (-1 = the default).
  */
 void moe_set_pair_gemm(int mask);

@@ -24,8 +24,15 @@
 //   computes h for the first 16 tokens of each 32-column step, the up warp
 //   for the other 16) and store h = act(g) * u.
 // Down GEMM: fb covers 256 rows of W_down[e] (H % 256 == 0), 128 per CTA;
-//   thread = output feature, the routing-weighted outputs are added into
-//   the fp32 accumulator row of each token (coalesced fp32 reductions).
+//   thread = output feature (TMEM lane).  Each 32-token step of a warp goes
+//   through a shared-memory transpose to token rows, and the
+//   routing-weighted outputs are added into the fp32 accumulator row of each
+//   token with 4-wide vector reductions (a lane: 4 consecutive features of
+//   one token).  With one scalar reduction and two shuffles per token and
+//   lane, the epilogue held the MMA back (its thread waited for a free
+//   accumulator 34-43 % of the time) and the pair lost to the one-CTA
+//   swap-AB kernel; with the transpose it wins from about 8 routed rows per
+//   expert.
 //
 // Stages cover 128 of K as two 64-wide swizzled slices: one TMA box per
 // operand and stage (the weights' [2E, I, K] view and the tokens' [n, K]
@@ -372,7 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const int col = t.fb * 256 + 128 * static_cast<int>(rank) + 32 * q + lane;
+        // Combine: per 32-token step the warp's 32 features x 32 tokens go
+        // through a shared-memory transpose (token rows of 32 floats), so a
+        // lane adds 4 consecutive features of one token with one vector
+        // reduction: 8 of them per step instead of 32 scalar ones.
+        float* stg = sX + q * 32 * 32;
+        const int col = t.fb * 256 + 128 * static_cast<int>(rank) + 32 * q + 4 * (lane & 7);
         for (int s = 0; s < nst; ++s) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tb + 32 * s, v);
@@ -386,14 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tok_l = fl / p.k;
             w_l = __ldg(p.topk_w + fl);
           }
+          __syncwarp();  // the previous step's reads of the staging tile are done
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int tok = __shfl_sync(0xffffffffu, tok_l, i);
-            const float w = __shfl_sync(0xffffffffu, w_l, i);
-            if (i < cnt) {
+          for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __uint_as_float(v[i]);
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int ti = 4 * j + (lane >> 3);  // token of this lane within the step
+            const int tok = __shfl_sync(0xffffffffu, tok_l, ti);
+            const float w = __shfl_sync(0xffffffffu, w_l, ti);
+            if (ti < cnt) {
+              const float4 y = *reinterpret_cast<const float4*>(stg + ti * 32 + 4 * (lane & 7));
               float* o = p.out32 + static_cast<long>(tok) * p.H + col;
-              if (p.l2_hints & 1) red_add_f32_hint(o, w * __uint_as_float(v[i]), pol_last);
-              else red_add_f32(o, w * __uint_as_float(v[i]));
+              if (p.l2_hints & 1) red_add_v4_hint(o, w * y.x, w * y.y, w * y.z, w * y.w, pol_last);
+              else red_add_v4(o, w * y.x, w * y.y, w * y.z, w * y.w);
             }
           }
         }

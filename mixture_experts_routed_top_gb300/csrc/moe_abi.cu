@@ -762,7 +762,7 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   const bool swap2 = g_swap_rows.load(std::memory_order_relaxed) >= 0 ? swap1 : true;
   // CTA-pair kernels (either GEMM, by the process-wide mask)
   const int pair_set = moe_get_pair_gemm();
-  const int pair = pair_set < 0 ? pair_gemm_default(H) : pair_set;
+  const int pair = pair_set < 0 ? pair_gemm_default(H, n, E) : pair_set;
   const bool pair1 = pair & 1;
   const bool pair2 = (pair & 2) && H % 256 == 0;
   // swap-AB kernel: 128-byte rows, token boxes of 64 rows; token-row

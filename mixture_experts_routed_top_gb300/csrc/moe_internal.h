@@ -146,13 +146,20 @@ cudaError_t launch_gemm2_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaSt
 // Default CTA-pair use (bit 0: gate/up, bit 1: down): gate/up on pairs for
 // H >= kPairGateUpMinH, measured faster there (DeepSeek-V3 width) and
 // slower at H = 2048 (Qwen width, whose ~140-token tiles leave the pair
-// bound by L2 reads); the down GEMM measured slower on pairs everywhere.
+// bound by L2 reads); the down GEMM on pairs from kPairDownMinRows routed
+// rows per expert on average (measured faster at every prefill size and at
+// 8.5 rows per expert, slower at 1.3 and 2.4, where the one-CTA swap-AB
+// kernel's 16-wide token tiles fit the batch).
 constexpr int kPairGateUpMinH = 4096;
+constexpr int kPairDownMinRows = 8;
 // Down GEMMs' L2 policies by default: the accumulator's reductions
 // evict_last (measured 1-3 % faster at every prefill size; evict_first on
 // the weight loads measured no faster and is off).
 constexpr int kDownL2Default = 1;
-inline int pair_gemm_default(int H) { return H >= kPairGateUpMinH ? 1 : 0; }
+inline int pair_gemm_default(int H, long n_rows, int E) {
+  return (H >= kPairGateUpMinH ? 1 : 0) |
+         (n_rows >= static_cast<long>(kPairDownMinRows) * E ? 2 : 0);
+}
 constexpr int kRowsBK = 64;  // K-block (bf16 elements) of the token-row kernel; 32 measured slower
 constexpr int kSwapRowsDefault = 128;  // mean rows per expert at or below: swap-AB kernel (measured)
 constexpr int kTileGroupDefault = 4;   // token-row gate/up: m-tiles per tile group (measured)
