@@ -91,6 +91,7 @@ struct PairDev {
   int act;
   int group;             // token tiles per tile group (0: all of the expert's)
   int l2_hints;          // down: bit 0 accumulator evict_last
+  int phases;            // down: feature-block slices run one after the other (>= 1)
 };
 
 struct Tile {
@@ -98,9 +99,17 @@ struct Tile {
 };
 
 // Tile -> (expert, feature block, token tile); s_pref = prefix of the
-// experts' token-tile counts ceil(M_e / 256).
+// experts' token-tile counts ceil(M_e / 256).  With phases > 1 the feature
+// blocks are cut into `phases` equal slices run one after the other (every
+// expert's tiles of slice 0, then of slice 1, ...), so the down GEMM's
+// combine touches a [T, H / phases] slice of the fp32 accumulator at a time.
 __device__ __forceinline__ Tile decode_tile(int tile, int NFB, int E, const int* s_off,
-                                            const int* s_pref, int group) {
+                                            const int* s_pref, int group, int phases = 1) {
+  const int nfp = NFB / phases;
+  const int per_phase = s_pref[E] * nfp;
+  const int ph = tile / per_phase;
+  tile -= ph * per_phase;
+  NFB = nfp;
   const int v = tile / NFB;
   int lo = 0, hi = E;
   while (lo < hi) {  // largest e with s_pref[e] <= v
@@ -118,6 +127,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NFB, int E, const int*
   const int r = local - g * G * NFB;
   t.fb = r / gg;
   const int j = g * G + (r - t.fb * gg);
+  t.fb += ph * nfp;
   const int M = s_off[lo + 1] - s_off[lo];
   const int b = static_cast<int>(static_cast<long>(j) * M / mt);  // sizes differ by <= 1
   const int en = static_cast<int>(static_cast<long>(j + 1) * M / mt);
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < total; tile += ncl) {
-        const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group);
+        const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group, p.phases);
         const int half = ((t.size + 15) & ~15) >> 1;
         const uint32_t tx = 2u * static_cast<uint32_t>(A_BYTES + B_BYTES);
         // gate/up: feature f0 of expert e in the [2E, I, H] view; down: the
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < total; tile += ncl, ++it) {
-        const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group);
+        const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group, p.phases);
         const int N = (t.size + 15) & ~15;  // <= 256
         const uint32_t idesc = idesc_bf16_f32(256, N);
         const int acc = it & 1;
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool odd = lane & 1;
     int it = 0, xs = 0;
     for (int tile = cid; tile < total; tile += ncl, ++it) {
-      const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group);
+      const Tile t = decode_tile(tile, NFB, E, s_off, s_pref, p.group, p.phases);
       const int acc = it & 1;
       int ok = 1;
       if (lane == 0)
@@ -473,6 +483,7 @@ cudaError_t launch_impl(const GroupedGemmArgs& a, long tiles_max, cudaStream_t s
   p.act = a.act;
   p.group = a.tile_group;
   p.l2_hints = a.l2_hints;
+  p.phases = (EPI == EPI_COMBINE && a.phases > 0) ? a.phases : 1;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

@@ -149,18 +149,22 @@ def test_forward_bf16_parity(moe, shape, path):
     assert np.all(np.isfinite(out))
 
 
+@pytest.mark.parametrize("pair", [0, 3], ids=["swap_down", "pair_down"])
 @pytest.mark.parametrize("phases", [2, 4])
-def test_forward_bf16_down_gemm_phases(moe, phases):
+def test_forward_bf16_down_gemm_phases(moe, phases, pair):
     """The down GEMM's output columns in 2 or 4 slices run one after the
-    other (the order used when the fp32 accumulator exceeds L2): every tile
-    still runs exactly once."""
+    other (the order used when the fp32 accumulator exceeds L2), on the
+    one-CTA swap-AB kernel and on CTA pairs: every tile still runs exactly
+    once."""
     from full_size_sampling import check_accumulator
     shape = MoEShape(T=300, H=1024, I=384, E=6, k=3)
     moe.set_down_phases(phases)
+    moe.set_pair_gemm(pair)
     try:
         out, ref = _forward_case(moe, shape)
     finally:
         moe.set_down_phases(-1)
+        moe.set_pair_gemm(-1)
     # 307 k outputs: checked on the fp32 accumulator, the bf16 output its
     # exact RNE image (see tests/full_size_sampling.py)
     out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
