@@ -1,6 +1,6 @@
 // Grouped tensor-core GEMMs (bf16), swap-AB orientation, for experts with
-// few routed rows (decode-sized batches; the token-row kernel in
-// gemm_rows.cu covers prefill).
+// few routed rows (decode-sized batches; prefill runs on the token-row
+// kernel in gemm_rows.cu or on CTA pairs in gemm_pair.cu).
 //
 // The expert's weight rows are the MMA's M side and its tokens the N side,
 // D[f, t] = W[f, :] . X[t, :].  A tile is (expert e, feature block fb,
