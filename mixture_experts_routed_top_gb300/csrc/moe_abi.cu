@@ -763,8 +763,11 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   // CTA-pair kernels (either GEMM, by the process-wide mask)
   const int pair_set = moe_get_pair_gemm();
   const int pair = pair_set < 0 ? pair_gemm_default(H, n, E) : pair_set;
-  const bool pair1 = pair & 1;
-  const bool pair2 = (pair & 2) && H % 256 == 0;
+  // the pair kernel takes 128 of K per stage (K = H for gate/up, I for
+  // down; the forward already requires both to be multiples of 128) and
+  // its down tiles are 256 output columns wide
+  const bool pair1 = (pair & 1) && H % 128 == 0;
+  const bool pair2 = (pair & 2) && H % 256 == 0 && I % 128 == 0;
   // swap-AB kernel: 128-byte rows, token boxes of 64 rows; token-row
   // kernel: rows of kRowsBK bf16, 128-row boxes for both operands; pair
   // kernel: 128-byte rows, 128-row token boxes, weight boxes of 64 rows

@@ -139,8 +139,9 @@ cudaError_t launch_gemm2_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 // The same GEMMs on CTA pairs (gemm_pair.cu: tcgen05.mma.cta_group::2,
 // M = 256 weight rows, tokens as N <= 256; tm_a = weights, tm_b =
 // activations with 64- (gate/up) or 128-row (down) weight boxes and 128-row
-// token boxes; the tile prefix is built in the
-// kernel; down needs H % 256 == 0).  n_rows = routed rows (T*k).
+// token boxes; the tile prefix is built in the kernel; stages cover 128 of
+// K, so K % 128 == 0, and down needs H % 256 == 0).  n_rows = routed rows
+// (T*k).
 cudaError_t launch_gemm1_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaStream_t s);
 cudaError_t launch_gemm2_bf16_pair(const GroupedGemmArgs& a, long n_rows, cudaStream_t s);
 // Default CTA-pair use (bit 0: gate/up, bit 1: down): gate/up on pairs for

@@ -140,6 +140,63 @@ SMALL_SHAPES = [
 ]
 
 
+def _random_shapes(n, seed):
+    """Seeded random shapes over the library's path boundaries: H and I
+    multiples of 128 (H with and without H % 256 == 0, which the CTA-pair
+    down GEMM needs), E up to 96, k up to 8, and T so that the
+    routed rows per expert run from under one (decode GEMVs) to a few
+    hundred (token-row and CTA-pair GEMMs, several ragged tiles)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = int(rng.integers(1, 97))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        per_expert = float(rng.choice([0.5, 2.0, 9.0, 40.0, 150.0, 320.0]))
+        T = max(1, min(700, int(round(per_expert * E / k))))
+        H = int(rng.choice([128, 256, 384, 512, 768, 1024]))
+        I = int(rng.choice([128, 256, 384, 512]))
+        out.append(MoEShape(T=T, H=H, I=I, E=E, k=k))
+    return out
+
+
+RANDOM_SHAPES = _random_shapes(16, seed=20261203)
+
+
+@pytest.mark.parametrize("shape", RANDOM_SHAPES, ids=lambda s: f"T{s.T}_H{s.H}_I{s.I}_E{s.E}_k{s.k}")
+def test_forward_bf16_random_shapes_default_paths(moe, shape):
+    """The library's own path choice (decode GEMVs, swap-AB, token-row or
+    CTA-pair GEMMs for either GEMM) on seeded random shapes, every output
+    against the oracle.  Above 100 k outputs the grouped paths are checked
+    on their fp32 accumulator, the bf16 output its exact RNE image: at that
+    many outputs the bf16 rounding of the largest ones alone approaches the
+    tolerance (see tests/full_size_sampling.py)."""
+    from full_size_sampling import check_accumulator
+    out, ref = _forward_case(moe, shape, seed=shape.T + shape.E)
+    assert np.all(np.isfinite(out))
+    grouped = shape.T * shape.k > moe.get_decode_rows()
+    if grouped and shape.T * shape.H > 100_000:
+        out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
+        check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
+    else:
+        err = O.rel_max_err(out, ref)
+        assert err <= BF16_TOL, (shape, err)
+
+
+@pytest.mark.parametrize("pair", [0, 3], ids=["one_cta", "cta_pairs"])
+def test_forward_bf16_random_shape_both_down_kernels_agree(moe, pair):
+    """The largest random shape through the one-CTA and the CTA-pair down
+    GEMMs: both within the tolerance on the fp32 accumulator."""
+    from full_size_sampling import check_accumulator
+    shape = max(RANDOM_SHAPES, key=lambda s: s.T * s.k * s.H)
+    moe.set_pair_gemm(pair)
+    try:
+        out, ref = _forward_case(moe, shape, seed=shape.T + shape.E)
+    finally:
+        moe.set_pair_gemm(-1)
+    out_t = torch.from_numpy(out).to(torch.bfloat16).cuda()
+    check_accumulator(moe, out_t, np.arange(shape.T), ref, shape, moe.W_BF16, BF16_TOL)
+
+
 @pytest.mark.parametrize("path", ["rows", "swap", "pair", "decode"], indirect=True)
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 def test_forward_bf16_parity(moe, shape, path):
