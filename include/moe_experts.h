@@ -179,8 +179,8 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_GELU = 1, MOE_ACT_RELU = 2 } moe_activa
 /*
  * moe_experts_forward_act - moe_experts_forward with the gate activation as
  * an argument; moe_experts_forward is this call with MOE_ACT_SILU.  Every
- * path (token-row and swap-AB grouped GEMMs, FP8, decode) applies it in the
- * gate/up epilogue.  An activation outside moe_activation:
+ * path (token-row, swap-AB and CTA-pair grouped GEMMs, FP8, FP4, decode)
+ * applies it in the gate/up epilogue.  An activation outside moe_activation:
  * MOE_ERR_INVALID_ARG.  Everything else as moe_experts_forward.
  */
 moe_status moe_experts_forward_act(const void* hidden, int T, int H,
@@ -259,8 +259,8 @@ void moe_set_swap_rows(int rows_per_expert);
 int moe_get_swap_rows(void);
 
 /*
- * moe_set_down_phases - tile order of the down GEMMs (bf16 swap-AB,
- * block-scaled and float32-scale FP8).  Their combine adds every routed row into the fp32
+ * moe_set_down_phases - tile order of the down GEMMs (bf16 on CTA pairs
+ * and swap-AB, block-scaled and float32-scale FP8).  Their combine adds every routed row into the fp32
  * accumulator [T, H] of its token; when that accumulator is larger than L2,
  * a token's k contributions, made by different experts at different times,
  * find its lines evicted.  With P phases the output columns are cut into P
@@ -290,8 +290,9 @@ void moe_set_pair_gemm(int mask);
 int moe_get_pair_gemm(void);
 
 /*
- * moe_set_down_l2_hints - L2 policies of the down GEMMs (bf16 swap-AB,
- * block-scaled and float32-scale FP8; bit 1 only the first two): bit 0 = the fp32 accumulator's reductions evict_last (its
+ * moe_set_down_l2_hints - L2 policies of the down GEMMs (bf16 on CTA pairs
+ * and swap-AB, block-scaled and float32-scale FP8; bit 1 only swap-AB and
+ * block-scaled): bit 0 = the fp32 accumulator's reductions evict_last (its
  * lines kept in preference to streaming data), bit 1 = the W_down tile
  * loads evict_first.  0: no policy; bits < 0 restore the default, 1 (the
  * accumulator evict_last, measured 1-3 % faster; bit 1 measured no faster).
