@@ -811,11 +811,11 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
     e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
                                : launch_dispatch(topk_idx, T, E, k, d, s);
     if (e != cudaSuccess) return cuda_fail(e, "dispatch");
-    if ((e = launch_gather_bf16(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), xa,
-                                s)) != cudaSuccess)
-      return cuda_fail(e, "gather");
-    if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
-      return cuda_fail(e, "zero out32");
+    // expert-sorted rows written from the token side (hidden read once), the
+    // fp32 accumulator zeroed in the same launch: at DeepSeek-V3 size 0.237
+    // against 0.317 ms for a row-side gather plus a zeroing kernel
+    if ((e = launch_scatter_rows_bf16(hidden, H, T, k, d.row_of, xa, out32, s)) != cudaSuccess)
+      return cuda_fail(e, "scatter");
   }
   GroupedGemmArgs g{};
   g.offsets = d.offsets;

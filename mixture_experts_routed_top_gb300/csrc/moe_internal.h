@@ -94,8 +94,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
                          cudaStream_t s);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const DispatchBufs& d,
                             cudaStream_t s);
-cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,
-                               const int* nvalid, int rows, void* x_perm, cudaStream_t s);
+// X_perm rows from the token side (row_of from the dispatch), and
+// out32[0:T*H] = 0 in the same launch.
+cudaError_t launch_scatter_rows_bf16(const void* hidden, int H, int T, int k, const int* row_of,
+                                     void* x_perm, float* out32, cudaStream_t s);
 cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
                               const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
                               cudaStream_t s);

@@ -244,43 +244,70 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
 }
 
 // ============================================================== gather
-// X_perm[r, :] = hidden[sorted_f[r] / k, :] for the rows the dispatch placed
-// (r < offsets[E]); one warp per row, 16-byte vectors, each lane loading
-// kGatherBatch vectors before storing them.
-constexpr int kGatherBatch = 8;
-__global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restrict__ hidden, int H8,
-                                                          int k, const int* __restrict__ sorted_f,
-                                                          const int* __restrict__ nvalid, int rows,
-                                                          uint4* __restrict__ xperm) {
+// X_perm written from the token side.  A warp owns one (token t, column
+// chunk of 32 B 16-byte vectors): it loads that piece of hidden[t] once and
+// stores it to the rows the dispatch placed t's k slots at (row_of[t*k + j];
+// -1 for a dropped slot), so hidden is read once rather than once per slot.
+// The same warp zeroes the matching columns of the token's fp32 accumulator
+// row out32[t, :], which the down GEMM's combine adds into.
+template <int B>
+__global__ void __launch_bounds__(128) scatter_rows_bf16_kernel(const uint4* __restrict__ hidden,
+                                                                int H8, int T, int k, int nchunks,
+                                                                const int* __restrict__ row_of,
+                                                                uint4* __restrict__ xperm,
+                                                                float4* __restrict__ out32) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (r >= rows || r >= *nvalid) return;
-  const long t = __ldg(sorted_f + r) / k;
+  const long w = static_cast<long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (w >= static_cast<long>(T) * nchunks) return;   // warp-uniform
+  const long t = w / nchunks;
+  const int c0 = static_cast<int>(w - t * nchunks) * (32 * B);
+  const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
   const uint4* src = hidden + t * H8;
-  uint4* dst = xperm + r * H8;
-  for (int c0 = lane; c0 < H8; c0 += 32 * kGatherBatch) {
-    uint4 v[kGatherBatch];
+  uint4 v[B];
 #pragma unroll
-    for (int i = 0; i < kGatherBatch; ++i) {
-      const int c = c0 + 32 * i;
-      v[i] = c < H8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-    }
+  for (int i = 0; i < B; ++i) {
+    const int c = c0 + 32 * i + lane;
+    v[i] = c < H8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int r = __shfl_sync(0xffffffffu, my_row, j);  // every lane reaches it
+    if (r < 0) continue;
+    uint4* dst = xperm + static_cast<long>(r) * H8;
 #pragma unroll
-    for (int i = 0; i < kGatherBatch; ++i) {
-      const int c = c0 + 32 * i;
+    for (int i = 0; i < B; ++i) {
+      const int c = c0 + 32 * i + lane;
       if (c < H8) __stcs(dst + c, v[i]);   // streaming: the rows are read back once
     }
   }
+  // fp32 columns [8 c0, 8 (c0 + 32 B)) = float4 [2 c0, 2 (c0 + 32 B))
+  float4* z = out32 + t * (2L * H8);
+  const int zend = min(2 * (c0 + 32 * B), 2 * H8);
+  for (int c = 2 * c0 + lane; c < zend; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-cudaError_t launch_gather_bf16(const void* hidden, int H, int k, const int* sorted_f,
-                               const int* nvalid, int rows, void* x_perm, cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  launch_pdl(gather_bf16_kernel, ceil_div(rows, 8), 256, 0, s, static_cast<const uint4*>(hidden), H / 8, k,
-                                                       sorted_f, nvalid, rows,
-                                                       static_cast<uint4*>(x_perm));
+// Chunk width: the widest (8, 4, 2 or 1 vectors per lane) that still gives
+// at least kScatterWarps warps, so small batches spread over many SMs.
+constexpr long kScatterWarps = 8192;
+
+cudaError_t launch_scatter_rows_bf16(const void* hidden, int H, int T, int k, const int* row_of,
+                                     void* x_perm, float* out32, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int H8 = H / 8;
+  int b = 8;
+  while (b > 1 && static_cast<long>(T) * ceil_div(H8, 32 * b) < kScatterWarps) b >>= 1;
+  const int nchunks = ceil_div(H8, 32 * b);
+  const int grid = ceil_div(static_cast<long>(T) * nchunks, 4);
+  const uint4* src = static_cast<const uint4*>(hidden);
+  uint4* dst = static_cast<uint4*>(x_perm);
+  float4* z = reinterpret_cast<float4*>(out32);
+  switch (b) {
+    case 8: launch_pdl(scatter_rows_bf16_kernel<8>, grid, 128, 0, s, src, H8, T, k, nchunks, row_of, dst, z); break;
+    case 4: launch_pdl(scatter_rows_bf16_kernel<4>, grid, 128, 0, s, src, H8, T, k, nchunks, row_of, dst, z); break;
+    case 2: launch_pdl(scatter_rows_bf16_kernel<2>, grid, 128, 0, s, src, H8, T, k, nchunks, row_of, dst, z); break;
+    default: launch_pdl(scatter_rows_bf16_kernel<1>, grid, 128, 0, s, src, H8, T, k, nchunks, row_of, dst, z); break;
+  }
   count_launches(1);
   return cudaGetLastError();
 }
