@@ -524,11 +524,9 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
                                  : launch_dispatch(topk_idx, T, E, k, d, s);
       if (e != cudaSuccess) return cuda_fail(e, "dispatch");
-      if ((e = launch_gather_quant_mx(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n),
-                                      fp4 ? 32 : 128, xq, xs, s)) != cudaSuccess)
-        return cuda_fail(e, "gather_quant_mx");
-      if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
-        return cuda_fail(e, "zero out32");
+      if ((e = launch_scatter_quant_mx(hidden, H, T, k, d.row_of, static_cast<int>(n),
+                                       fp4 ? 32 : 128, xq, xs, out32, s)) != cudaSuccess)
+        return cuda_fail(e, "scatter_quant_mx");
     }
     GroupedGemmMxArgs g{};
     g.offsets = d.offsets;
@@ -698,11 +696,8 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
       e = n <= kSmallDispatchMax ? launch_dispatch_small(topk_idx, T, E, k, d, s)
                                  : launch_dispatch(topk_idx, T, E, k, d, s);
       if (e != cudaSuccess) return cuda_fail(e, "dispatch");
-      if ((e = launch_gather_fp8(hidden, H, k, d.sorted_f, d.offsets + E, static_cast<int>(n), ue,
-                                 xq, xs, s)) != cudaSuccess)
-        return cuda_fail(e, "gather_fp8");
-      if ((e = launch_zero_f32(out32, static_cast<long>(T) * H, s)) != cudaSuccess)
-        return cuda_fail(e, "zero out32");
+      if ((e = launch_scatter_fp8(hidden, H, T, k, d.row_of, ue, xq, xs, out32, s)) != cudaSuccess)
+        return cuda_fail(e, "scatter_fp8");
     }
     GroupedGemmFp8Args g{};
     g.offsets = d.offsets;

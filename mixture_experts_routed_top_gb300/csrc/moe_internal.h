@@ -98,12 +98,10 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
 // out32[0:T*H] = 0 in the same launch.
 cudaError_t launch_scatter_rows_bf16(const void* hidden, int H, int T, int k, const int* row_of,
                                      void* x_perm, float* out32, cudaStream_t s);
-cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
-                              const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
-                              cudaStream_t s);
-// out[0:n] = 0 (n a multiple of 4), as a kernel so it takes part in the
-// programmatic launch chain.
-cudaError_t launch_zero_f32(float* out, long n, cudaStream_t s);
+// FP8 activations (1x128 blocks, scales row-major) from the token side,
+// and out32[0:T*H] = 0 in the same launch.
+cudaError_t launch_scatter_fp8(const void* hidden, int H, int T, int k, const int* row_of,
+                               bool ue8m0, uint8_t* xq, void* xs, float* out32, cudaStream_t s);
 cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s);
 cudaError_t launch_quantize_blocks(const void* w, int nmat, int rows, int cols, bool ue8m0,
                                    uint8_t* q, void* scale, cudaStream_t s);
@@ -234,11 +232,12 @@ struct GroupedGemmMxArgs {
 };
 cudaError_t launch_gemm1_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
 cudaError_t launch_gemm2_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s);
-// Gather + e4m3 quantisation of the routed rows in 1 x block UE8M0 blocks
-// (block 128 or 32), scale words K-block-major as above.
-cudaError_t launch_gather_quant_mx(const void* hidden, int H, int k, const int* sorted_f,
-                                   const int* nvalid, int rows, int block, uint8_t* xq,
-                                   uint32_t* xs, cudaStream_t s);
+// e4m3 quantisation of the routed rows in 1 x block UE8M0 blocks (block 128
+// or 32), written from the token side, scale words K-block-major as above;
+// out32[0:T*H] = 0 in the same launch.
+cudaError_t launch_scatter_quant_mx(const void* hidden, int H, int T, int k, const int* row_of,
+                                    int rows, int block, uint8_t* xq, uint32_t* xs, float* out32,
+                                    cudaStream_t s);
 
 // Small-token decode path.
 struct DecodeArgs {

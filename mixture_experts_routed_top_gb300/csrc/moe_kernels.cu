@@ -319,102 +319,95 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Gather + dynamic 1x128 activation quantisation: one warp per row; each
-// half-warp quantises one 128-wide block (16 lanes x 8 elements), and a lane
-// issues the loads of four blocks (eight per warp) before any arithmetic.
-// Codes go to xq[r, :], scales to xs[r, b] with a row stride of
-// scale_stride(H/128) blocks (a multiple of 4, so that one vector load
-// fetches four blocks' scales).
-__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ hidden, int H,
-                                                         int k, const int* __restrict__ sorted_f,
-                                                         const int* __restrict__ nvalid, int rows,
-                                                         bool ue8m0, uint2* __restrict__ xq,
-                                                         void* __restrict__ xs) {
+// Dynamic 1x128 activation quantisation written from the token side: a warp
+// owns one token and 8 of its 128-wide blocks (a half-warp per block, 16
+// lanes x 8 elements, four blocks per half-warp), quantises them once and
+// stores codes and scales to the rows the dispatch placed the token's k
+// slots at (row_of[t*k + j], -1 for a dropped slot).  Codes go to xq[r, :],
+// scales to xs[r, b] with a row stride of scale_stride(H/128) blocks (a
+// multiple of 4, so that one vector load fetches four blocks' scales).  The
+// same warp zeroes the matching columns of the token's fp32 accumulator row.
+__global__ void __launch_bounds__(128) scatter_fp8_kernel(const uint4* __restrict__ hidden, int H,
+                                                          int T, int k, int nchunks,
+                                                          const int* __restrict__ row_of,
+                                                          bool ue8m0, uint2* __restrict__ xq,
+                                                          void* __restrict__ xs,
+                                                          float4* __restrict__ out32) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
-  const long r = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (r >= rows || r >= *nvalid) return;
-  const long t = __ldg(sorted_f + r) / k;
+  const long w = static_cast<long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (w >= static_cast<long>(T) * nchunks) return;   // warp-uniform
+  const long t = w / nchunks;
+  const int b0 = static_cast<int>(w - t * nchunks) * 8;
   const int nb = H / 128;
   const long sstride = scale_stride(nb);
+  const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
   const uint4* src = hidden + t * (H / 8);
-  uint2* dst = xq + r * (H / 8);
-  for (int b0 = 0; b0 < nb; b0 += 8) {
-    uint4 raw[4];
+  uint4 raw[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int b = b0 + 2 * i + half;
-      raw[i] = b < nb ? __ldg(src + b * 16 + l16) : make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < 4; ++i) {
+    const int b = b0 + 2 * i + half;
+    raw[i] = b < nb ? __ldg(src + b * 16 + l16) : make_uint4(0, 0, 0, 0);
+  }
+  uint2 code[4];
+  uint32_t stored[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float x[8];
+    const uint32_t wd[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(wd[j] << 16);
+      x[2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
     }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)  // stays inside the half-warp
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = block_scale(amax, ue8m0, &stored[i]);
+    const float inv = 1.0f / sc;
+    code[i] = make_uint2(e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16),
+                         e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16));
+  }
+  for (int j = 0; j < k; ++j) {
+    const int r = __shfl_sync(0xffffffffu, my_row, j);  // every lane reaches it
+    if (r < 0) continue;
+    uint2* dst = xq + static_cast<long>(r) * (H / 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int b = b0 + 2 * i + half;
-      float x[8];
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[2 * j] = __uint_as_float(w[j] << 16);
-        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1)  // stays inside the half-warp
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      uint32_t stored;
-      const float sc = block_scale(amax, ue8m0, &stored);
-      const float inv = 1.0f / sc;
       if (b < nb) {
-        const uint32_t c0 = e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16);
-        const uint32_t c1 = e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16);
-        dst[b * 16 + l16] = make_uint2(c0, c1);
+        dst[b * 16 + l16] = code[i];
         if (l16 == 0) {
           const long si = r * sstride + b;
-          if (ue8m0) static_cast<uint8_t*>(xs)[si] = static_cast<uint8_t>(stored);
-          else static_cast<uint32_t*>(xs)[si] = stored;
+          if (ue8m0) static_cast<uint8_t*>(xs)[si] = static_cast<uint8_t>(stored[i]);
+          else static_cast<uint32_t*>(xs)[si] = stored[i];
         }
       }
     }
   }
+  // fp32 columns of blocks [b0, b0 + 8): float4 [32 b0, 32 min(b0 + 8, nb))
+  float4* z = out32 + t * (H / 4);
+  const int zend = 32 * min(b0 + 8, nb);
+  for (int c = 32 * b0 + lane; c < zend; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-cudaError_t launch_gather_fp8(const void* hidden, int H, int k, const int* sorted_f,
-                              const int* nvalid, int rows, bool ue8m0, uint8_t* xq, void* xs,
-                              cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  launch_pdl(gather_fp8_kernel, ceil_div(rows, 8), 256, 0, s, static_cast<const uint4*>(hidden), H, k,
-                                                      sorted_f, nvalid, rows, ue8m0,
-                                                      reinterpret_cast<uint2*>(xq), xs);
+cudaError_t launch_scatter_fp8(const void* hidden, int H, int T, int k, const int* row_of,
+                               bool ue8m0, uint8_t* xq, void* xs, float* out32, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int nchunks = ceil_div(H / 128, 8);
+  launch_pdl(scatter_fp8_kernel, ceil_div(static_cast<long>(T) * nchunks, 4), 128, 0, s,
+             static_cast<const uint4*>(hidden), H, T, k, nchunks, row_of, ue8m0,
+             reinterpret_cast<uint2*>(xq), xs, reinterpret_cast<float4*>(out32));
   count_launches(1);
   return cudaGetLastError();
 }
 
 // ============================================================== finish
-// out[0:4*n4] = 0.
-__global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ out, long n4) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
-  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
-    out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-cudaError_t launch_zero_f32(float* out, long n, cudaStream_t s) {
-  const long n4 = n / 4;
-  if (n4 == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long want = (n4 + 255) / 256;
-  const long cap = static_cast<long>(sms > 0 ? sms : 148) * 8;
-  const int grid = static_cast<int>(want < cap ? want : cap);
-  count_launches(1);
-  return launch_pdl(zero_f32_kernel, grid, 256, 0, s, reinterpret_cast<float4*>(out), n4);
-}
-
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src,
                                                       uint2* __restrict__ dst, long n4) {
   pdl_launch_dependents();
