@@ -506,93 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ------------------------------------------------------------ activations
-// Dynamic e4m3 quantisation of the routed rows with UE8M0 scales in 1 x BLK
-// blocks (BLK = 128 for FP8 experts, 32 for FP4 experts), written from the
-// token side: a warp owns one token and 8 of its 128-wide K blocks (a
-// half-warp per block, 16 lanes x 8 elements, four blocks per half-warp),
-// quantises them once and stores the codes and scale words to the rows the
-// dispatch placed the token's k slots at (row_of[t*k + j], -1 for a dropped
-// slot).  Codes go to xq[r, :], scale words (four sub-block bytes per
-// 128-wide block, each byte the scale of its 32-wide sub-block) to
-// xs[kb * rows + r].  The same warp zeroes the matching columns of the
-// token's fp32 accumulator row.
-template <int BLK>
-__global__ void __launch_bounds__(128) scatter_quant_mx_kernel(const uint4* __restrict__ hidden,
-                                                               int H, int T, int k, int nchunks,
-                                                               const int* __restrict__ row_of,
-                                                               int rows, uint2* __restrict__ xq,
-                                                               uint32_t* __restrict__ xs,
-                                                               float4* __restrict__ out32) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, l16 = lane & 15;
-  const long w = static_cast<long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  if (w >= static_cast<long>(T) * nchunks) return;   // warp-uniform
-  const long t = w / nchunks;
-  const int b0 = static_cast<int>(w - t * nchunks) * 8;
-  const int nb = H / 128;
-  const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
-  const uint4* src = hidden + t * (H / 8);
-  uint4 raw[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int b = b0 + 2 * i + half;
-    raw[i] = b < nb ? __ldg(src + b * 16 + l16) : make_uint4(0, 0, 0, 0);
-  }
-  uint2 code[4];
-  uint32_t word[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float x[8];
-    const uint32_t wd[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = __uint_as_float(wd[j] << 16);
-      x[2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
-    // lanes of one block: 16 (BLK = 128) or 4 (BLK = 32), inside the half-warp
-#pragma unroll
-    for (int off = BLK / 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    uint32_t sb;
-    const float sc = block_scale(amax, true, &sb);
-    const float inv = 1.0f / sc;
-    // scale word of the 128-wide block: byte j = sub-block j's exponent
-    if (BLK == 128) {
-      word[i] = sb * 0x01010101u;
-    } else {
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 4);
-      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 8);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 12);
-      word[i] = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-    }
-    code[i] = make_uint2(e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16),
-                         e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16));
-  }
-  for (int j = 0; j < k; ++j) {
-    const int r = __shfl_sync(0xffffffffu, my_row, j);  // every lane reaches it
-    if (r < 0) continue;
-    uint2* dst = xq + static_cast<long>(r) * (H / 8);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int b = b0 + 2 * i + half;
-      if (b < nb) {
-        dst[b * 16 + l16] = code[i];
-        if (l16 == 0) xs[static_cast<long>(b) * rows + r] = word[i];
-      }
-    }
-  }
-  // fp32 columns of blocks [b0, b0 + 8): float4 [32 b0, 32 min(b0 + 8, nb))
-  float4* z = out32 + t * (H / 4);
-  const int zend = 32 * min(b0 + 8, nb);
-  for (int c = 32 * b0 + lane; c < zend; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 template <int EPI, bool FP4W>
 cudaError_t launch_mx_impl(const GroupedGemmMxArgs& a, cudaStream_t s) {
   auto kern = grouped_gemm_mx_kernel<EPI, FP4W>;
@@ -640,19 +553,6 @@ cudaError_t launch_gemm1_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s
 
 cudaError_t launch_gemm2_mx(const GroupedGemmMxArgs& a, bool fp4, cudaStream_t s) {
   return fp4 ? launch_mx_impl<EPI_COMBINE, true>(a, s) : launch_mx_impl<EPI_COMBINE, false>(a, s);
-}
-
-cudaError_t launch_scatter_quant_mx(const void* hidden, int H, int T, int k, const int* row_of,
-                                    int rows, int block, uint8_t* xq, uint32_t* xs, float* out32,
-                                    cudaStream_t s) {
-  if (T == 0) return cudaSuccess;
-  const int nchunks = ceil_div(H / 128, 8);
-  const int grid = ceil_div(static_cast<long>(T) * nchunks, 4);
-  auto kern = block == 32 ? scatter_quant_mx_kernel<32> : scatter_quant_mx_kernel<128>;
-  launch_pdl(kern, grid, 128, 0, s, static_cast<const uint4*>(hidden), H, T, k, nchunks, row_of,
-             rows, reinterpret_cast<uint2*>(xq), xs, reinterpret_cast<float4*>(out32));
-  count_launches(1);
-  return cudaGetLastError();
 }
 
 }  // namespace moe
