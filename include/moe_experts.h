@@ -358,7 +358,7 @@ int moe_get_fp4_gemv_rows(void);
  * (index = moe_stage); it returns the number of stages.  Not thread-safe.
  */
 typedef enum {
-  MOE_STAGE_DISPATCH = 0, /* histogram, scan, permute, gather (+ quantise) */
+  MOE_STAGE_DISPATCH = 0, /* histogram, scan, permute, sorted-row copy    */
   MOE_STAGE_GEMM1 = 1,    /* gate/up projection + SwiGLU                   */
   MOE_STAGE_GEMM2 = 2,    /* down projection + weighted combine             */
   MOE_STAGE_FINISH = 3,   /* fp32 -> bf16 output                            */

@@ -493,8 +493,9 @@ moe_status moe_experts_forward_act(const void* hidden, int T, int H, const int32
   const bool mx = (fp8 && sfmt == MOE_SCALE_UE8M0 && moe_get_block_scaled_mma()) || fp4_gemm;
   if (mx) {
     // FP8 (UE8M0) or FP4 experts on the tensor core's block scaling:
-    // dispatch, gather + e4m3 quantisation of the rows in 1x128 (FP8) or 1x32
-    // (FP4) blocks, the two block-scaled grouped GEMMs, bf16 output
+    // dispatch, e4m3 quantisation of the rows in 1x128 (FP8) or 1x32 (FP4)
+    // blocks written in expert order (accumulator zeroed in the same launch),
+    // the two block-scaled grouped GEMMs, bf16 output
     uint8_t* xq = w + L.xa;
     uint32_t* xs = reinterpret_cast<uint32_t*>(w + L.xa_scale);
     uint8_t* hq = w + L.hb;

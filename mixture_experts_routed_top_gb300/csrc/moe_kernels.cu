@@ -1,5 +1,7 @@
-// Router, dispatch, gather, output conversion and FP8 block quantisation
-// kernels (everything except the grouped tensor-core GEMMs).
+// Router, dispatch, the expert-sorted row copies (bf16, or e4m3 with their
+// block scales; each also zeroes the fp32 accumulator), output conversion
+// and FP8 weight quantisation kernels (everything except the grouped
+// tensor-core GEMMs and the decode GEMVs).
 #include <cuda_fp8.h>
 #include <float.h>
 #include <limits.h>
