@@ -111,8 +111,9 @@ def test_dominant_roof_is_the_one_that_binds():
     """The roofline time is max(flops / tensor peak, bytes / HBM bandwidth):
     the Qwen-shaped gate/up GEMM (E=60, every expert touched) moves more
     bytes than its flops take at the tensor peak, the DeepSeek-V3-shaped one
-    the reverse; decode batches stream weights."""
-    peaks = {"hbm_gbs": 6705.2, "bf16_tflops": 1886.7}
+    the reverse; decode batches stream weights.  The tensor peak is the
+    sustained measurement (the timed loops run back to back)."""
+    peaks = {"hbm_gbs": 6705.2, "bf16_tflops": 1886.7, "bf16_tflops_sustained": 1737.5}
 
     def roof(sname, T, wfmt, sfmt, dominant, touched):
         w = _w(sname, T, wfmt, sfmt)
@@ -126,7 +127,7 @@ def test_dominant_roof_is_the_one_that_binds():
     assert f == 4.0 * s.H * s.I * s.T * s.k
     # weights (gate and up rows of 60 experts), X rows in, h rows out
     assert b == 60 * 2 * s.H * s.I * 2 + s.T * s.k * (s.H + s.I) * 2
-    assert hbm and pk == 1886.7
+    assert hbm and pk == 1737.5
     (f, b, wb, pk, hbm), s = roof("dsv3", 8192, "bf16", None, "gemm1", 192)
     assert not hbm
     (f, b, wb, pk, hbm), s = roof("dsv3", 8192, "bf16", None, "gemm2", 192)
@@ -134,4 +135,4 @@ def test_dominant_roof_is_the_one_that_binds():
     (f, b, wb, pk, hbm), s = roof("qwen", 32, "bf16", None, "gemm1", 50)
     assert hbm
     (f, b, wb, pk, hbm), s = roof("dsv3_fp8", 16384, "fp8", "f32", "gemm1", 214)
-    assert not hbm and pk == 2 * 1886.7
+    assert not hbm and pk == 2 * 1737.5
