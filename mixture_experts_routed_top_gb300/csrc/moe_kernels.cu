@@ -253,7 +253,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
 // The same warp zeroes the matching columns of the token's fp32 accumulator
 // row out32[t, :], which the down GEMM's combine adds into.
 template <int B>
-__global__ void __launch_bounds__(128, B >= 8 ? 12 : 16) scatter_rows_bf16_kernel(const uint4* __restrict__ hidden,
+__global__ void __launch_bounds__(128, B >= 8 ? 9 : 16) scatter_rows_bf16_kernel(const uint4* __restrict__ hidden,
                                                                 int H8, int T, int k, int nchunks,
                                                                 const int* __restrict__ row_of,
                                                                 uint4* __restrict__ xperm,
@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(128, B >= 8 ? 12 : 16) scatter_rows_bf16_kerne
 
 // Chunk width: the widest (8, 4, 2 or 1 vectors per lane) that still gives
 // at least kScatterWarps warps, so small batches spread over many SMs; with
-// at most 4 vectors a lane the kernel fits 16 blocks (64 warps) per SM.
+// at most 4 vectors a lane the kernel fits 16 blocks (64 warps) per SM; the
+// 8-vector form gets 9 (capped at 12 it spilled).
 // Measured at Qwen prefill size (T = 4096, H = 2048): 16384 warps (1 KB
 // chunks) 30.1-30.3 us for the dispatch stage, 8192 warps 31.1 us, 4096
 // warps 33.2-33.6 us; decode sizes the same either way.
