@@ -514,24 +514,29 @@ cudaError_t launch_scatter_quant_mx(const void* hidden, int H, int T, int k, con
 }
 
 // ============================================================== finish
+// out[8 i .. 8 i + 7] = bf16(src[8 i .. 8 i + 7]): per thread and step two
+// 16-byte loads in flight and one 16-byte store.
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src,
-                                                      uint2* __restrict__ dst, long n4) {
+                                                      uint4* __restrict__ dst, long n8) {
   pdl_launch_dependents();
   pdl_wait();
-  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
-    const float4 v = __ldg(src + i);
-    dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    const float4 a = __ldg(src + 2 * i);
+    const float4 b = __ldg(src + 2 * i + 1);
+    dst[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                        pack_bf16x2(b.z, b.w));
   }
 }
 
 cudaError_t launch_to_bf16(const float* src, void* dst, long n, cudaStream_t s) {
-  const long n4 = n / 4;
-  if (n4 == 0) return cudaSuccess;
-  const long want = (n4 + 255) / 256;
+  if (n % 8 != 0) return cudaErrorInvalidValue;  // n = T * H, H a multiple of 128
+  const long n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const long want = (n8 + 255) / 256;
   const int grid = static_cast<int>(want < 152L * 16 ? want : 152L * 16);
   launch_pdl(to_bf16_kernel, grid, 256, 0, s, reinterpret_cast<const float4*>(src),
-                                      reinterpret_cast<uint2*>(dst), n4);
+             reinterpret_cast<uint4*>(dst), n8);
   count_launches(1);
   return cudaGetLastError();
 }
