@@ -253,6 +253,22 @@ def dominant_roof(w, dominant, flops, wbytes, peaks):
     return kern_flops, kern_bytes, kern_wbytes, pk, hbm_bound
 
 
+def roof_entry(w, hbm_bound, kern_flops, kern_bytes, d_avg_s, pk, peaks):
+    """The dominant kernel against the roof that binds it: its algorithmic
+    bytes or flops per launch over its average launch time.  Tensor-bound
+    entries are against `pk` (the sustained rate, from dominant_roof) and
+    carry the fraction of the burst rate beside it."""
+    if hbm_bound:
+        achieved = kern_bytes / d_avg_s / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    achieved = kern_flops / d_avg_s / 1e12
+    pk_burst = peaks["bf16_tflops"] * tensor_ratio(w)
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
+            "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
+            "frac_of_burst": round(achieved / pk_burst, 4), "peak_burst": pk_burst}
+
+
 def algorithmic(w, counts):
     """Algorithmic flops and bytes of one step (routed rows only; weight bytes
     of the experts that received rows; hidden in, logits in, output out)."""
@@ -619,16 +635,7 @@ def run_ours(args, rank, world, local_rank):
     d_avg_s = d_ms / max(d_n, 1) / 1e3
     kern_flops, kern_bytes, kern_wbytes, pk, hbm_bound = dominant_roof(w, dominant, flops, wbytes,
                                                                       peaks)
-    if hbm_bound:
-        achieved = kern_bytes / d_avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        achieved = kern_flops / d_avg_s / 1e12
-        pk_burst = peaks["bf16_tflops"] * tensor_ratio(w)
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
-                "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
-                "frac_of_burst": round(achieved / pk_burst, 4), "peak_burst": pk_burst}
+    roof = roof_entry(w, hbm_bound, kern_flops, kern_bytes, d_avg_s, pk, peaks)
     peak_kind = ("hbm_gbs, STREAM-style copy" if hbm_bound else
                  "bf16 sustained: the kernel runs inside a loop of back-to-back steps"
                  if w["wfmt"] == "bf16" else

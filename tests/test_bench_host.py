@@ -136,3 +136,36 @@ def test_dominant_roof_is_the_one_that_binds():
     assert hbm
     (f, b, wb, pk, hbm), s = roof("dsv3_fp8", 16384, "fp8", "f32", "gemm1", 214)
     assert not hbm and pk == 2 * 1737.5
+
+
+def test_roof_entry_reports_sustained_and_burst_fractions():
+    """Tensor-bound lines: achieved = flops per launch / launch time, against
+    the sustained rate, with the burst fraction beside it (x2 for the
+    FP8-rate MMAs); HBM-bound lines against the copy bandwidth."""
+    peaks = {"hbm_gbs": 6705.2, "bf16_tflops": 1886.7, "bf16_tflops_sustained": 1737.5}
+    w = _w("dsv3", 8192, "bf16", None)
+    s = w["shape"]
+    counts = np.zeros(s.E, np.int64)
+    counts[:194] = 1                 # the bench workload's touched experts
+    flops, wbytes, _, _ = bench.algorithmic(w, counts)
+    f, b, _, pk, hbm = bench.dominant_roof(w, "gemm1", flops, wbytes, peaks)
+    r = bench.roof_entry(w, hbm, f, b, 3.364e-3, pk, peaks)
+    assert r["bound"] == "tensor" and r["peak"] == 1737.5 and r["peak_burst"] == 1886.7
+    assert abs(r["achieved"] - f / 3.364e-3 / 1e12) < 0.06
+    assert abs(r["frac"] - r["achieved"] / 1737.5) < 1e-4
+    assert abs(r["frac_of_burst"] - r["achieved"] / 1886.7) < 1e-4
+    w8 = _w("dsv3_fp8", 16384, "fp8", "ue8m0")
+    c8 = np.zeros(w8["shape"].E, np.int64)
+    c8[:205] = 1
+    f8, wb8, _, _ = bench.algorithmic(w8, c8)
+    f, b, _, pk, hbm = bench.dominant_roof(w8, "gemm1", f8, wb8, peaks)
+    r = bench.roof_entry(w8, hbm, f, b, 3.76e-3, pk, peaks)
+    assert r["peak"] == 2 * 1737.5 and r["peak_burst"] == 2 * 1886.7
+    wq = _w("qwen", 4096, "bf16", None)
+    cq = np.ones(wq["shape"].E, np.int64)
+    fq, wbq, _, _ = bench.algorithmic(wq, cq)
+    f, b, _, pk, hbm = bench.dominant_roof(wq, "gemm1", fq, wbq, peaks)
+    r = bench.roof_entry(wq, hbm, f, b, 0.195e-3, pk, peaks)
+    assert hbm and r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - b / 0.195e-3 / 1e9 / 6705.2) < 1e-4
+    assert "frac_of_burst" not in r
