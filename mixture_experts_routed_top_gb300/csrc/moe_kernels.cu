@@ -245,7 +245,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
   return cudaGetLastError();
 }
 
-// ============================================================== gather
+// ============================================================== expert-sorted rows
 // X_perm written from the token side.  A warp owns one (token t, column
 // chunk of 32 B 16-byte vectors): it loads that piece of hidden[t] once and
 // stores it to the rows the dispatch placed t's k slots at (row_of[t*k + j];
@@ -253,11 +253,10 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int E, int k, const 
 // The same warp zeroes the matching columns of the token's fp32 accumulator
 // row out32[t, :], which the down GEMM's combine adds into.
 template <int B>
-__global__ void __launch_bounds__(128, B >= 8 ? 9 : 16) scatter_rows_bf16_kernel(const uint4* __restrict__ hidden,
-                                                                int H8, int T, int k, int nchunks,
-                                                                const int* __restrict__ row_of,
-                                                                uint4* __restrict__ xperm,
-                                                                float4* __restrict__ out32) {
+__global__ void __launch_bounds__(128, B >= 8 ? 9 : 16)
+    scatter_rows_bf16_kernel(const uint4* __restrict__ hidden, int H8, int T, int k, int nchunks,
+                             const int* __restrict__ row_of, uint4* __restrict__ xperm,
+                             float4* __restrict__ out32) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
